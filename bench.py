@@ -1,0 +1,486 @@
+#!/usr/bin/env python
+"""Benchmark: sink+window attention over the 30-layer rolling KV cache stack.
+
+Workload (default ``stream30``): Wan2.1-1.3B-shaped self-attention -- 30 layers,
+12 heads of dimension 128, 1560 tokens per latent frame, chunks of 3 frames,
+a 3-frame sink and a 9-frame window, bf16.  One step = one whole stream from an
+empty cache: 20 chunks (60 latent frames), each chunk attended and committed in
+all 30 layers (600 ll_attend_chunk calls with commit; independent seeded q/k/v
+per layer and chunk, all resident in HBM before timing starts: 25.9 GB, well
+above the 126 MB L2, so no flush is needed between steps).  The warm-up chunks
+attend to 3, 6, 9 and 12 frames, the rest to 15 (23400 keys); the first FIFO
+eviction happens at the commit of chunk 4.
+
+Printed (rank 0, one JSON line): latent frames/s of the stack (all ranks),
+TFLOPS, the attend kernel's roofline against the measured bf16 peak, the
+append kernel's HBM bandwidth, an end-to-end number with host<->device copies,
+the float64 oracle's CPU throughput on a bounded sample, and sampled clocks.
+
+``--impl reference`` times the float64 CPU oracle instead (the only
+reference implementation there is), on bounded samples of the same workload.
+Multi-GPU (torchrun): every rank runs its own independent stream (weak
+scaling, no collective on the data path); timing is max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import llsynth  # noqa: E402
+
+METRIC = "sink+window attention TFLOPS & latent frames/s (30-layer stack); % bf16 peak"
+UNIT = "latent_frames/s"
+FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+
+# ----------------------------------------------------------------------------
+# workload arithmetic (what counts as algorithmic work)
+# ----------------------------------------------------------------------------
+
+def resident_count(S, W, n):
+    return min(S, n) + min(W, max(0, n - S))
+
+
+def stream_plan(shape: llsynth.Shape, chunks: int):
+    """Per chunk: (t0, keys attended).  Work counts only the keys the method attends."""
+    T, C = shape.tokens_per_frame, shape.chunk_frames
+    plan = []
+    for c in range(chunks):
+        t0 = c * C
+        plan.append((t0, (resident_count(shape.sink_frames, shape.window_frames, t0) + C) * T))
+    return plan
+
+
+def attend_flops(Lq, Lkv, H, d):
+    return 4.0 * Lq * Lkv * H * d
+
+
+def append_bytes(shape: llsynth.Shape, frames_written: int):
+    """K and V: read from the chunk tensors and written to the cache, per committed frame."""
+    return 2 * 2 * frames_written * shape.tokens_per_frame * shape.heads * shape.head_dim * 2
+
+
+def frames_written(shape: llsynth.Shape, t0: int):
+    S, W, C = shape.sink_frames, shape.window_frames, shape.chunk_frames
+    lo = max(S, t0 + C - W)
+    return sum(1 for f in range(t0, t0 + C) if f < S or f >= lo)
+
+
+# ----------------------------------------------------------------------------
+# environment: distributed, peaks, clocks
+# ----------------------------------------------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while work runs."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q, "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("ll_attend_tc.cu", "ll_internal.h"):
+        with open(os.path.join(ROOT, "windowed_sink_attention_ll_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_per_launch():
+    """DRAM bytes per attend launch from the committed ncu summary, if it matches this source."""
+    p = os.path.join(ROOT, "profiles", "attend_tc_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------
+# CPU baseline: the float64 oracle on a bounded sample
+# ----------------------------------------------------------------------------
+
+def oracle_rate(shape: llsynth.Shape, budget_s: float = 12.0):
+    """Attention flop/s of the float64 oracle on one steady-state attend (sampled rows)."""
+    import numpy as np
+
+    import oracle
+
+    try:
+        from threadpoolctl import threadpool_info
+
+        threads = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        threads = os.cpu_count()
+    H, d, T, S, W, C = (shape.heads, shape.head_dim, shape.tokens_per_frame, shape.sink_frames,
+                        shape.window_frames, shape.chunk_frames)
+    orc = oracle.OracleCache(1, H, d, T, S, W, C)
+    rng = np.random.default_rng(0)
+    L = C * T
+    z = rng.standard_normal((L, H, d))
+    steady = S + W
+    while orc.state(0)[0] < steady:
+        orc.commit(0, z, z)
+    q = rng.standard_normal((L, H, d))
+    Lkv = (resident_count(S, W, orc.state(0)[0]) + C) * T
+    rows, done_rows, spent = 16, 0, 0.0
+    while True:
+        sel = np.arange(rows) * (L // rows)
+        t = time.perf_counter()
+        orc.attend(0, q, z, z, commit=False, rows=sel)
+        dt = time.perf_counter() - t
+        spent += dt
+        done_rows += rows
+        left = budget_s - spent
+        if left < 0.6 * dt:
+            break
+        # size the next call to fit what is left of the budget
+        rows = int(max(16, min(L, rows * left / dt * 0.8)))
+    rate = attend_flops(done_rows, Lkv, H, d) / spent
+    sample = ("float64 oracle attend of %d sampled query rows (all %d heads, %d keys) of a steady-state "
+              "chunk, %.1f s; rate scaled by the step's attention flops" % (done_rows, H, Lkv, spent))
+    return rate, threads, sample
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+
+def run_ours(args, world, rank, local):
+    import windowed_sink_attention_ll_b300 as ll
+
+    shape = llsynth.STREAM30
+    chunks = llsynth.STREAM30_CHUNKS
+    H, d, T, S, W, C = (shape.heads, shape.head_dim, shape.tokens_per_frame, shape.sink_frames,
+                        shape.window_frames, shape.chunk_frames)
+    L = C * T
+    plan = stream_plan(shape, chunks)
+    step_frames = chunks * C
+    step_flops = sum(attend_flops(L, lkv, H, d) for _, lkv in plan) * shape.layers
+    step_append = sum(append_bytes(shape, frames_written(shape, t0)) for t0, _ in plan) * shape.layers
+
+    # inputs: independent seeded q/k/v per (rank, layer, chunk), resident before timing
+    inputs = [[tuple(llsynth.seeded_normal(("bench", rank, l, c, t), (L, H, d), device="cuda") for t in "qkv")
+               for c in range(chunks)] for l in range(shape.layers)]
+    outs = [torch.empty((L, H, d), dtype=torch.bfloat16, device="cuda") for _ in range(shape.layers)]
+    cache = ll.ll_cache_create(shape.layers, H, d, T, S, W, C, ll.LL_BF16)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ll.ll_reset(cache)
+        for c in range(chunks):
+            for l in range(shape.layers):
+                q, k, v = inputs[l][c]
+                ll.ll_attend_chunk(cache, l, q, k, v, outs[l], True, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    for kind in (ll.LL_KERNEL_ATTEND, ll.LL_KERNEL_COPY, ll.LL_KERNEL_PREFILL):
+        ll.ll_profile_read(cache, kind)
+    ll.ll_profile_enable(cache, True)
+    launches0 = ll.ll_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ll.ll_profile_enable(cache, False)
+    launches = ll.ll_launch_count() - launches0
+    ms = ev0.elapsed_time(ev1)
+    ms_max = max_over_ranks(ms, world)
+    n_att, ms_att = ll.ll_profile_read(cache, ll.LL_KERNEL_ATTEND)
+    n_cp, ms_cp = ll.ll_profile_read(cache, ll.LL_KERNEL_COPY)
+
+    pk, pk_src = peaks()
+    tflops_att = step_flops * args.steps / (ms_att / 1e3) / 1e12
+    peak_t = pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
+    gbs_cp = step_append * args.steps / (ms_cp / 1e3) / 1e9
+    traffic = traffic_per_launch()
+    result = {
+        "metric": METRIC,
+        "value": step_frames * args.steps * world / (ms_max / 1e3),
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_max / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v per layer and chunk, Wan2.1-1.3B shapes; no weights)",
+        "config": {"workload": "stream30: 30 layers x 20 chunks (60 latent frames), H=12, d=128, "
+                               "T=1560, C=3, S=3, W=9, 1 committed pass per chunk",
+                   "layers": shape.layers, "chunks": chunks, "heads": H, "head_dim": d,
+                   "tokens_per_frame": T, "sink_frames": S, "window_frames": W, "chunk_frames": C,
+                   "l2": "inputs larger than L2 (%.1f GB q/k/v + %.2f GB cache per rank)" % (
+                       3 * L * H * d * 2 * chunks * shape.layers / 1e9, 2 * shape.layers * (S + W) * T * H * d * 2 / 1e9),
+                   "parallelism": "replicas x%d (independent streams, no collective)" % world},
+        "tflops": step_flops * args.steps * world / (ms_max / 1e3) / 1e12,
+        "roofline": {"kernel": "attend_tc_kernel<128>", "bound": "tensor", "achieved": tflops_att,
+                     "peak": peak_t, "unit": "TFLOP/s", "frac": tflops_att / peak_t,
+                     "peak_source": "%s bf16_tflops_sustained (kernel timed inside a long step)" % pk_src,
+                     "frac_of_burst_peak": tflops_att / pk.get("bf16_tflops", FALLBACK["bf16_tflops"]),
+                     "frac_of_nominal_2250": tflops_att / 2250.0,
+                     "launches": n_att, "ms_per_launch": ms_att / max(n_att, 1),
+                     "flops_per_launch": step_flops * args.steps / max(n_att, 1),
+                     "traffic": traffic},
+        "append": {"kernel": "copy_frames_kernel", "bound": "hbm", "achieved": gbs_cp,
+                   "peak": pk.get("hbm_gbs", FALLBACK["hbm_gbs"]), "unit": "GB/s",
+                   "frac": gbs_cp / pk.get("hbm_gbs", FALLBACK["hbm_gbs"]), "frac_of_nominal_8000": gbs_cp / 8000.0,
+                   "launches": n_cp, "us_per_launch": 1e3 * ms_cp / max(n_cp, 1),
+                   "bytes_per_launch": step_append * args.steps / max(n_cp, 1)},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(ll, cache, shape, chunks, step_frames, world, rank, args)
+    cache.close()
+    del inputs
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, threads, sample = oracle_rate(shape)
+        result["cpu_baseline"] = {"value": step_frames / (step_flops / rate), "unit": UNIT, "cores": threads,
+                                  "kind": "oracle", "sample": sample}
+    return result
+
+
+def run_e2e(ll, cache, shape, chunks, step_frames, world, rank, args):
+    """Same stream through the public API with q/k/v copied in from pinned host memory and every
+    output copied back, double-buffered on copy streams."""
+    H, d, T, C = shape.heads, shape.head_dim, shape.tokens_per_frame, shape.chunk_frames
+    L = C * T
+    pool = 4  # distinct pinned host input sets, cycled
+    host_in = [tuple(llsynth.seeded_normal(("bench-e2e", rank, i, t), (L, H, d)).pin_memory() for t in "qkv")
+               for i in range(pool)]
+    host_out = [torch.empty((L, H, d), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    dev_in = [tuple(torch.empty((L, H, d), dtype=torch.bfloat16, device="cuda") for _ in range(3)) for _ in range(2)]
+    dev_out = [torch.empty((L, H, d), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    comp = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    done = [torch.cuda.Event() for _ in range(2)]
+    drained = [torch.cuda.Event() for _ in range(2)]
+    for e in done + drained:
+        e.record(comp)
+    bytes_in = bytes_out = 0
+
+    def step():
+        nonlocal bytes_in, bytes_out
+        ll.ll_reset(cache)
+        i = 0
+        for c in range(chunks):
+            for l in range(shape.layers):
+                b = i % 2
+                src = host_in[i % pool]
+                s_in.wait_event(done[b])
+                with torch.cuda.stream(s_in):
+                    for dst, h in zip(dev_in[b], src):
+                        dst.copy_(h, non_blocking=True)
+                ready = torch.cuda.Event()
+                ready.record(s_in)
+                comp.wait_event(ready)
+                comp.wait_event(drained[b])
+                ll.ll_attend_chunk(cache, l, *dev_in[b], dev_out[b], True, comp)
+                done[b].record(comp)
+                s_out.wait_event(done[b])
+                with torch.cuda.stream(s_out):
+                    host_out[b].copy_(dev_out[b], non_blocking=True)
+                drained[b].record(s_out)
+                bytes_in += 3 * L * H * d * 2
+                bytes_out += L * H * d * 2
+                i += 1
+
+    step()
+    torch.cuda.synchronize()
+    bytes_in = bytes_out = 0
+    steps = max(1, min(args.steps, 2))
+    barrier(world)
+    torch.cuda.synchronize()
+    t = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    el = max_over_ranks(time.perf_counter() - t, world)
+    barrier(world)
+    return {"value": step_frames * steps * world / el, "unit": UNIT, "steps": steps,
+            "h2d_bytes_per_step": bytes_in // steps, "d2h_bytes_per_step": bytes_out // steps,
+            "how": "pinned host q/k/v -> device (copy stream) -> ll_attend_chunk -> out -> pinned host "
+                   "(copy stream), double-buffered; wall clock"}
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the float64 oracle, on bounded samples of the same workload
+# ----------------------------------------------------------------------------
+
+def run_reference(args, world, rank):
+    shape = llsynth.STREAM30
+    chunks = llsynth.STREAM30_CHUNKS
+    H, d, T, C = shape.heads, shape.head_dim, shape.tokens_per_frame, shape.chunk_frames
+    L = C * T
+    plan = stream_plan(shape, chunks)
+    step_frames = chunks * C
+    step_flops = sum(attend_flops(L, lkv, H, d) for _, lkv in plan) * shape.layers
+    budget = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_rate(shape, budget_s=min(budget, 3.0))
+    times, rates, threads, sample = [], [], 1, ""
+    for _ in range(args.steps):
+        rate, threads, sample = oracle_rate(shape, budget_s=budget)
+        rates.append(rate)
+        times.append(step_flops / rate)
+    ms_step = 1e3 * statistics.mean(times)
+    value = step_frames / (ms_step / 1e3)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "stream30: 30 layers x 20 chunks (60 latent frames), H=12, d=128, T=1560, "
+                               "C=3, S=3, W=9 (float64 CPU oracle, sampled rows; step time scaled by flops)"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        # CPU-only arm: rank 0 alone times the oracle; other ranks exit without work
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        if rank == 0:
+            print(json.dumps(run_reference(args, world, rank)), flush=True)
+        return
+    world, rank, local = dist_setup()
+    res = run_ours(args, world, rank, local)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

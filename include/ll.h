@@ -1,0 +1,198 @@
+/*
+ * ll.h -- C ABI of the short-window + frame-sink attention library (sm_103a).
+ *
+ * Operation (from "LongLive: Real-time Interactive Long Video Generation",
+ * §3.3 Efficient Long Inference, "Short window attention" and "Frame sink";
+ * §3.1 KV Recache; §4 Implementation; §4.4 Table 4):
+ *
+ *   A causal, chunk-by-chunk video generator keeps, per transformer layer, a
+ *   KV cache of latent frames.  The first S frames (the first frame chunk) are
+ *   a sink that is never evicted; the other cached frames form a rolling
+ *   window of the W most recent frames, evicted first-in first-out.  A chunk
+ *   of C frames (C*T query tokens) attends, per head, to
+ *       [sink frames' K/V || window frames' K/V || the chunk's own K/V]
+ *   with softmax(Q K^T / sqrt(d)) V and no mask inside that list.  When a
+ *   pass commits, the chunk's K/V enter the cache (evicting the oldest
+ *   window frames).  At a prompt switch the resident frames' K/V are
+ *   recomputed ("recache") and written back in place.
+ *
+ * Conventions for every call:
+ *   - Shapes: T = tokens_per_frame, C = chunk_frames, S = sink_frames,
+ *     W = window_frames, H = heads, d = head_dim (64 or 128).
+ *   - Token tensors (q, k, v, out, *_win) are caller-owned DEVICE pointers,
+ *     contiguous [tokens][H][d] in the cache dtype (bf16 or fp32), 16-byte
+ *     aligned.  They are borrowed until the work enqueued on `stream`
+ *     completes.  No call keeps a pointer after that.
+ *   - Calls on one cache are not thread-safe.  Host metadata (frames
+ *     committed, frame-to-slot map) is updated when a call is enqueued, so
+ *     calls must be issued in stream order on a single stream.
+ *   - Argument and state errors are detected on the host before anything is
+ *     enqueued; the call then returns the error and changes nothing.
+ *   - Kernel launch failures return LL_ERR_CUDA.  A device-side wait that
+ *     runs out of time sets an error word that the next call (or
+ *     ll_cache_state / ll_sync) reports as LL_ERR_DEVICE_TIMEOUT.
+ *   - No call synchronises the device except ll_cache_read, ll_sync and
+ *     ll_cache_state (which checks the device error word).
+ */
+#ifndef LL_H_
+#define LL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LL_API __attribute__((visibility("default")))
+#else
+#define LL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ll_cache ll_cache; /* opaque */
+
+/* Element type of the cache and of every token tensor. */
+typedef enum { LL_BF16 = 0, LL_FP32 = 1 } ll_dtype;
+
+typedef enum {
+  LL_OK = 0,
+  LL_ERR_INVALID_ARG = 1,   /* bad shape, null or misaligned pointer, layer out of range */
+  LL_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement (e.g. d not 64/128) */
+  LL_ERR_OOM = 3,           /* device allocation failed in ll_cache_create */
+  LL_ERR_STATE = 4,         /* call not allowed in the cache's state (e.g. recache of an empty layer) */
+  LL_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed */
+  LL_ERR_DEVICE_TIMEOUT = 6 /* a bounded device-side wait gave up (reported by a later call) */
+} ll_status;
+
+/* Human-readable name of a status code (static storage). */
+LL_API const char* ll_status_str(ll_status s);
+
+/*
+ * ll_cache_create -- allocate the per-layer KV caches.
+ * §3.3 "Short window attention": the cache is sized by the window, not by the
+ * video length: K and V each hold layers * H * (S + W) * T * d elements,
+ * head-major [layer][head][slot][token][d].  The memory is cudaMalloc'ed on
+ * the current device and zero-filled; ll_cache_destroy frees it.
+ * Requirements: layers, heads, tokens_per_frame, chunk_frames >= 1;
+ * sink_frames, window_frames >= 0; head_dim in {64, 128}.  Returns
+ * LL_ERR_OOM if the allocation fails (then *out is NULL).
+ */
+LL_API ll_status ll_cache_create(ll_cache** out, int layers, int heads, int head_dim,
+                          int tokens_per_frame, int sink_frames, int window_frames,
+                          int chunk_frames, ll_dtype dtype);
+
+/* Free the cache (waits for the device to finish with it).  NULL is ignored. */
+LL_API void ll_cache_destroy(ll_cache* cache);
+
+/*
+ * ll_attend_chunk -- one query pass of the chunk that starts at frame
+ * t0 = frames committed so far in `layer`.
+ * §3.3 "Frame sink" + "Short window attention": per head h,
+ *   out_h = softmax(q_h K_h^T / sqrt(d)) V_h,
+ *   K/V = [frames 0..min(S,t0)-1 || frames max(S,t0-W)..t0-1 || k/v of this chunk].
+ * q, k, v, out: [C*T][H][d] device buffers (out may not alias q, k or v).
+ * commit != 0: after the attention, the chunk's K/V are written into the
+ * cache: frame f < S into sink slot f, frame f >= S into ring slot
+ * S + ((f - S) mod W), replacing the frame W positions older; frames that
+ * would be evicted within the same commit (W < C) are not written.  Frames
+ * committed += C.  Softmax statistics are fp32; out is rounded to the dtype.
+ */
+LL_API ll_status ll_attend_chunk(ll_cache* cache, int layer, const void* q, const void* k,
+                          const void* v, void* out, int commit, void* stream);
+
+/*
+ * ll_recache -- §3.1 "KV recache": replace the K/V of the R frames resident
+ * in `layer` (R = min(S,n) + min(W, max(0, n - S)), n = frames committed) by
+ * k_win/v_win, [R*T][H][d], given in list order (sink frames ascending, then
+ * window frames ascending).  Frame indices and n do not change.
+ * Returns LL_ERR_STATE if the layer is empty (n = 0).
+ */
+LL_API ll_status ll_recache(ll_cache* cache, int layer, const void* k_win, const void* v_win,
+                     void* stream);
+
+/*
+ * ll_recache_attend -- the recache prefill: block-causal attention over the
+ * R resident frames' fresh q/k/v (list cut into blocks of C frames; query
+ * rows of block g see key blocks 0..g), written to out_win [R*T][H][d];
+ * then the same K/V write as ll_recache.
+ */
+LL_API ll_status ll_recache_attend(ll_cache* cache, int layer, const void* q_win, const void* k_win,
+                            const void* v_win, void* out_win, void* stream);
+
+/* §4.4 Table 4 ("no KV cache"): drop every frame of every layer (metadata only). */
+LL_API ll_status ll_reset(ll_cache* cache);
+
+/*
+ * ll_cache_state -- host copy of one layer's bookkeeping: frames committed and
+ * frame_of_slot[S + W] (-1 = empty slot).  Synchronises the device first and
+ * returns LL_ERR_DEVICE_TIMEOUT if a device-side wait gave up since the last
+ * check.  Either output pointer may be NULL.
+ */
+LL_API ll_status ll_cache_state(ll_cache* cache, int layer, int64_t* frames_committed,
+                         int64_t* frame_of_slot);
+
+/*
+ * ll_cache_read -- copy one layer's raw cache to HOST buffers, each
+ * H * (S + W) * T * d elements in the head-major slot layout (for tests;
+ * synchronises the device).
+ */
+LL_API ll_status ll_cache_read(ll_cache* cache, int layer, void* host_k, void* host_v);
+
+/* Wait for all work on the device; report a pending device error, if any. */
+LL_API ll_status ll_sync(ll_cache* cache);
+
+/* Sizes of a cache: S + W slots, bytes of one layer's K (same for V), element size. */
+LL_API ll_status ll_cache_info(const ll_cache* cache, int* slots, size_t* layer_bytes, int* elem_bytes);
+
+/*
+ * Host-side index logic, exported for tests (no device needed):
+ * ll_frame_slot: slot of frame f (-1 if f can not be resident, i.e. f >= S and W = 0).
+ * ll_resident_frames: frames resident after n commits in list order
+ * (sink asc, window asc) into frames[] (capacity >= S + W); returns the count.
+ */
+LL_API int ll_frame_slot(int sink_frames, int window_frames, int64_t f);
+LL_API int ll_resident_frames(int sink_frames, int window_frames, int64_t n, int64_t* frames);
+
+/*
+ * Number of kernel launches this library has made since it was loaded
+ * (all caches, all devices).  Benchmarks read it to count launches.
+ */
+LL_API uint64_t ll_launch_count(void);
+
+/*
+ * Per-kernel timing.  While profiling is on, each kernel this cache launches is
+ * bracketed by two CUDA events on its stream.  ll_profile_read synchronises,
+ * returns for one kernel kind the number of launches and their summed device
+ * time (milliseconds) since profiling was switched on, and clears that kind.
+ */
+typedef enum {
+  LL_KERNEL_ATTEND = 0,  /* chunk attention (tensor-core or fp32 kernel) */
+  LL_KERNEL_PREFILL = 1, /* recache prefill attention */
+  LL_KERNEL_COPY = 2,    /* commit / recache K,V write */
+  LL_KERNEL_KINDS = 3
+} ll_kernel_kind;
+LL_API ll_status ll_profile_enable(ll_cache* cache, int enable);
+LL_API ll_status ll_profile_read(ll_cache* cache, int kind, int64_t* launches, double* total_ms);
+
+/*
+ * Test hook: a non-zero value makes the next tensor-core attention launch of
+ * this cache skip one barrier arrival so its bounded waits run out after
+ * `timeout_us` microseconds; the kernel then returns early and the next call
+ * reports LL_ERR_DEVICE_TIMEOUT.  0 disarms it.  The fp32 kernel has no
+ * barriers and ignores it.
+ */
+LL_API ll_status ll_debug_inject_stall(ll_cache* cache, int enable, int timeout_us);
+
+/*
+ * Test hook: a non-zero value routes this cache's bf16 attention through the
+ * CUDA-core kernel that serves the fp32 dtype (one warp per query row) instead
+ * of the tensor-core kernel, so tests can compare the two CUDA kernels.
+ */
+LL_API ll_status ll_debug_use_simt(ll_cache* cache, int enable);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LL_H_ */

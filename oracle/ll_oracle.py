@@ -223,13 +223,24 @@ class OracleCache:
             self._commit(layer, k, v)
         return out
 
+    def commit(self, layer: int, k, v) -> None:
+        """The state change of a committing pass, for passes whose outputs nobody reads.
+
+        Frames are kept as views of the given arrays (converted to float64);
+        callers must not modify them afterwards.
+        """
+        k = np.asarray(k, dtype=np.float64)
+        v = np.asarray(v, dtype=np.float64)
+        assert k.shape == (self.C * self.T, self.H, self.d) and v.shape == k.shape
+        self._commit(layer, k, v)
+
     def _commit(self, layer: int, k: np.ndarray, v: np.ndarray) -> None:
         lay = self.layers[layer]
         T = self.T
         t0 = lay.n
         for i in range(self.C):
             f = t0 + i
-            lay.frames[f] = (k[i * T:(i + 1) * T].copy(), v[i * T:(i + 1) * T].copy())
+            lay.frames[f] = (k[i * T:(i + 1) * T], v[i * T:(i + 1) * T])
         lay.n = t0 + self.C
         keep = set(resident_frames(self.S, self.W, lay.n))
         for f in list(lay.frames):
@@ -251,7 +262,7 @@ class OracleCache:
         v_win = np.asarray(v_win, dtype=np.float64)
         assert k_win.shape == (len(frames) * T, self.H, self.d) and v_win.shape == k_win.shape
         for i, f in enumerate(frames):
-            lay.frames[f] = (k_win[i * T:(i + 1) * T].copy(), v_win[i * T:(i + 1) * T].copy())
+            lay.frames[f] = (k_win[i * T:(i + 1) * T], v_win[i * T:(i + 1) * T])
 
     def recache_attend(self, layer: int, q_win, k_win, v_win, rows=None) -> np.ndarray:
         """Recache with the prefill attention: block-causal over the resident list.

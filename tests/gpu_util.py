@@ -1,0 +1,137 @@
+"""Helpers of the GPU parity tests: a GPU cache driven in lock-step with the oracle."""
+
+import numpy as np
+import torch
+
+import oracle
+
+# Tolerance of the attention outputs against the float64 oracle with bf16
+# inputs (same for fp32): max |err| <= 1e-2 and relative L2 <= 5e-3.
+ATOL = 1e-2
+REL_L2 = 5e-3
+
+
+def f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().double().cpu().numpy()
+
+
+def compare(got: torch.Tensor, want: np.ndarray, what: str, atol=ATOL, rel_l2=REL_L2):
+    g = f64(got)
+    assert g.shape == want.shape, (what, g.shape, want.shape)
+    assert np.isfinite(g).all(), what + ": non-finite output"
+    err = float(np.abs(g - want).max())
+    rel = float(np.linalg.norm(g - want) / max(np.linalg.norm(want), 1e-30))
+    assert err <= atol and rel <= rel_l2, "%s: max|err| %.3e (<= %g), rel_l2 %.3e (<= %g)" % (
+        what, err, atol, rel, rel_l2)
+    return err, rel
+
+
+def sample_rows(L: int, n: int, seed: int = 0) -> np.ndarray:
+    """Deterministic query-row sample: both ends, tile edges, the ragged tail, random rest."""
+    fixed = {0, 1, 127, 128, 255, 256, 383, 384, L - 1, L - 2, (L // 128) * 128, (L // 256) * 256 - 1}
+    fixed = {r for r in fixed if 0 <= r < L}
+    rng = np.random.default_rng(seed)
+    rest = rng.choice(L, size=min(L, max(0, n - len(fixed))), replace=False)
+    return np.array(sorted(fixed | set(int(r) for r in rest)), dtype=np.int64)
+
+
+def bits(t: torch.Tensor) -> torch.Tensor:
+    return t.view(torch.int16) if t.element_size() == 2 else t.view(torch.int32)
+
+
+class Lockstep:
+    """A libll cache and an oracle cache fed the same calls; checks state after each one.
+
+    ``host`` keeps, per layer and frame, the exact K/V values the GPU was given
+    (CPU tensors), so the raw cache bytes can be compared slot by slot.
+    """
+
+    def __init__(self, ll, layers, heads, head_dim, T, S, W, C, dtype, keep_frames=True):
+        self.ll = ll
+        self.cache = ll.ll_cache_create(layers, heads, head_dim, T, S, W, C, dtype)
+        self.orc = oracle.OracleCache(layers, heads, head_dim, T, S, W, C)
+        self.shape = (layers, heads, head_dim, T, S, W, C)
+        self.dtype = dtype
+        self.keep = keep_frames
+        self.host = [dict() for _ in range(layers)]
+        self._zeros = None
+
+    @property
+    def T(self):
+        return self.shape[3]
+
+    @property
+    def C(self):
+        return self.shape[6]
+
+    def attend(self, layer, q, k, v, commit, rows=None, check=True, what=""):
+        """q, k, v: CUDA tensors.  Returns the GPU output (and checks it unless check=False)."""
+        out = torch.empty_like(q)
+        self.ll.ll_attend_chunk(self.cache, layer, q, k, v, out, commit)
+        if check:
+            qh, kh, vh = f64(q), f64(k), f64(v)
+            want = self.orc.attend(layer, qh, kh, vh, commit, rows=rows)
+            got = out if rows is None else out[torch.as_tensor(rows, device=out.device)]
+            compare(got, want, what or "attend")
+        elif commit:
+            kh, vh = f64(k), f64(v)
+            self.orc.commit(layer, kh, vh)
+        if commit and self.keep:
+            t0 = self.orc.state(layer)[0] - self.C
+            kc, vc = k.cpu(), v.cpu()
+            for i in range(self.C):
+                self.host[layer][t0 + i] = (kc[i * self.T:(i + 1) * self.T], vc[i * self.T:(i + 1) * self.T])
+        return out
+
+    def commit_placeholder(self, layer, q, k, v):
+        """GPU gets the real chunk; the oracle a zero chunk.
+
+        For chunks whose frames no checked output can see: if the GPU kept such a
+        frame by mistake, the checked outputs would differ from the oracle's.
+        """
+        out = torch.empty_like(q)
+        self.ll.ll_attend_chunk(self.cache, layer, q, k, v, out, True)
+        if self._zeros is None or self._zeros.shape != tuple(q.shape):
+            self._zeros = np.zeros(tuple(q.shape))
+        self.orc.commit(layer, self._zeros, self._zeros)
+        return out
+
+    def recache(self, layer, k_win, v_win):
+        self.ll.ll_recache(self.cache, layer, k_win, v_win)
+        self.orc.recache(layer, f64(k_win), f64(v_win))
+        self._keep_recache(layer, k_win, v_win)
+
+    def recache_attend(self, layer, q_win, k_win, v_win, rows=None, check=True, what=""):
+        out = torch.empty_like(q_win)
+        self.ll.ll_recache_attend(self.cache, layer, q_win, k_win, v_win, out)
+        if check:
+            want = self.orc.recache_attend(layer, f64(q_win), f64(k_win), f64(v_win), rows=rows)
+            got = out if rows is None else out[torch.as_tensor(rows, device=out.device)]
+            compare(got, want, what or "recache prefill")
+        else:
+            self.orc.recache(layer, f64(k_win), f64(v_win))
+        self._keep_recache(layer, k_win, v_win)
+        return out
+
+    def _keep_recache(self, layer, k_win, v_win):
+        if not self.keep:
+            return
+        kc, vc = k_win.cpu(), v_win.cpu()
+        for i, f in enumerate(self.orc.resident(layer)):
+            self.host[layer][f] = (kc[i * self.T:(i + 1) * self.T], vc[i * self.T:(i + 1) * self.T])
+
+    def check_state(self, layers=None):
+        for layer in range(self.shape[0]) if layers is None else layers:
+            got = self.ll.ll_cache_state(self.cache, layer)
+            assert got == self.orc.state(layer), (layer, got, self.orc.state(layer))
+
+    def check_raw(self, layer):
+        """Every occupied slot holds, bit for bit, the K/V the oracle says it holds."""
+        hk, hv = self.ll.ll_cache_read(self.cache, layer)
+        for slot, f in self.orc.expected_slots(layer).items():
+            k, v = self.host[layer][f]
+            assert torch.equal(bits(hk[:, slot]), bits(k.permute(1, 0, 2).contiguous())), (layer, slot, f)
+            assert torch.equal(bits(hv[:, slot]), bits(v.permute(1, 0, 2).contiguous())), (layer, slot, f)
+
+    def close(self):
+        self.cache.close()

@@ -1,0 +1,119 @@
+"""CPU-only checks of the C-ABI library: it builds, loads, exports every symbol the
+header declares, and its host-side index logic matches the oracle bit for bit."""
+
+import os
+import re
+
+import pytest
+import torch
+
+import oracle
+from tests.conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def ll():
+    from windowed_sink_attention_ll_b300 import build_lib
+
+    build_lib.build()
+    import windowed_sink_attention_ll_b300 as mod
+
+    mod._lib()
+    return mod
+
+
+def header_symbols():
+    text = open(os.path.join(ROOT, "include", "ll.h")).read()
+    return sorted(set(re.findall(r"^LL_API [^(]*?\b(ll_\w+)\(", text, flags=re.M)))
+
+
+def test_library_exports_every_declared_symbol(ll):
+    declared = header_symbols()
+    assert len(declared) >= 16
+    lib = ll._lib()
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert sorted(ll.EXPORTS) == declared
+
+
+def test_binding_names_match_the_abi(ll):
+    for name in header_symbols():
+        assert callable(getattr(ll, name)), name
+
+
+def test_frame_slot_matches_oracle(ll):
+    for S in range(0, 6):
+        for W in range(0, 8):
+            for f in range(0, 60):
+                want = oracle.slot_of_frame(S, W, f) if (f < S or W > 0) else -1
+                assert ll.ll_frame_slot(S, W, f) == want
+
+
+def test_resident_frames_match_oracle(ll):
+    for S in range(0, 6):
+        for W in range(0, 8):
+            for n in range(0, 80):
+                assert ll.ll_resident_frames(S, W, n) == oracle.resident_frames(S, W, n)
+
+
+def test_resident_slots_form_a_prefix(ll):
+    # the kernels read resident keys as slots [0, R): check that claim for many shapes
+    for S in range(0, 6):
+        for W in range(0, 8):
+            for C in range(1, 5):
+                for n in range(0, 60, C):
+                    frames = ll.ll_resident_frames(S, W, n)
+                    slots = sorted(ll.ll_frame_slot(S, W, f) for f in frames)
+                    assert slots == list(range(len(frames)))
+
+
+def test_status_strings(ll):
+    assert [ll.ll_status_str(i) for i in range(7)] == ll.STATUS
+
+
+def test_create_rejects_bad_arguments_before_touching_a_device(ll):
+    bad = [
+        (0, 2, 64, 16, 3, 6, 3, ll.LL_BF16),
+        (1, 0, 64, 16, 3, 6, 3, ll.LL_BF16),
+        (1, 2, 64, 0, 3, 6, 3, ll.LL_BF16),
+        (1, 2, 64, 16, -1, 6, 3, ll.LL_BF16),
+        (1, 2, 64, 16, 3, -1, 3, ll.LL_BF16),
+        (1, 2, 64, 16, 3, 6, 0, ll.LL_BF16),
+        (1, 2, 64, 16, 3, 6, 3, 7),
+    ]
+    for args in bad:
+        with pytest.raises(ll.LLError) as e:
+            ll.ll_cache_create(*args)
+        assert e.value.status == ll.LL_ERR_INVALID_ARG, args
+    for args in [(1, 2, 96, 16, 3, 6, 3, ll.LL_BF16), (1, 2, 64, 16, 400, 200, 3, ll.LL_BF16)]:
+        with pytest.raises(ll.LLError) as e:
+            ll.ll_cache_create(*args)
+        assert e.value.status == ll.LL_ERR_UNSUPPORTED, args
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
+def test_create_without_a_device_fails_cleanly(ll):
+    with pytest.raises(ll.LLError) as e:
+        ll.ll_cache_create(1, 2, 64, 16, 3, 6, 3, ll.LL_BF16)
+    assert e.value.status == ll.LL_ERR_CUDA
+
+
+def test_null_handle_calls_return_invalid_arg(ll):
+    lib = ll._lib()
+    assert lib.ll_reset(None) == ll.LL_ERR_INVALID_ARG
+    assert lib.ll_sync(None) == ll.LL_ERR_INVALID_ARG
+    assert lib.ll_attend_chunk(None, 0, None, None, None, None, 0, None) == ll.LL_ERR_INVALID_ARG
+    assert lib.ll_recache(None, 0, None, None, None) == ll.LL_ERR_INVALID_ARG
+    assert lib.ll_recache_attend(None, 0, None, None, None, None, None) == ll.LL_ERR_INVALID_ARG
+    assert lib.ll_cache_state(None, 0, None, None) == ll.LL_ERR_INVALID_ARG
+    assert lib.ll_cache_read(None, 0, None, None) == ll.LL_ERR_INVALID_ARG
+    assert lib.ll_cache_info(None, None, None, None) == ll.LL_ERR_INVALID_ARG
+    assert lib.ll_debug_inject_stall(None, 1, 10) == ll.LL_ERR_INVALID_ARG
+    lib.ll_cache_destroy(None)
+
+
+def test_binding_rejects_host_tensors(ll):
+    cache = ll.LLCache(None, 1, 2, 64, 16, 3, 6, 3, ll.LL_BF16)
+    t = torch.zeros(48, 2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ll.ll_attend_chunk(cache, 0, t, t, t, t, True)

@@ -1,0 +1,272 @@
+"""Python binding of libll, the sm_103a short-window + frame-sink attention library.
+
+Thin ctypes marshalling over the C ABI in ``include/ll.h``: every function here
+has the name of the C entry point it calls, checks the tensors it is given
+(device, dtype, shape, contiguity), passes raw device pointers and the current
+CUDA stream, and turns a non-OK status into :class:`LLError`.  All compute runs
+in the library's CUDA kernels; there is no fallback.  PyTorch only supplies
+device memory and streams.
+
+The operation ("LongLive: Real-time Interactive Long Video Generation", §3.3
+Efficient Long Inference and §3.1 KV Recache): a per-layer KV cache holding S
+sink frames that are never evicted plus a rolling window of the W most recent
+frames; a chunk of C frames attends to [sink || window || its own K/V] and,
+when it commits, enters the window with FIFO eviction; a prompt switch
+recomputes the resident frames' K/V in place.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libll.so")
+
+LL_BF16, LL_FP32 = 0, 1
+STATUS = ["LL_OK", "LL_ERR_INVALID_ARG", "LL_ERR_UNSUPPORTED", "LL_ERR_OOM", "LL_ERR_STATE",
+          "LL_ERR_CUDA", "LL_ERR_DEVICE_TIMEOUT"]
+(LL_OK, LL_ERR_INVALID_ARG, LL_ERR_UNSUPPORTED, LL_ERR_OOM, LL_ERR_STATE, LL_ERR_CUDA,
+ LL_ERR_DEVICE_TIMEOUT) = range(7)
+
+# every symbol include/ll.h declares
+EXPORTS = ("ll_status_str", "ll_cache_create", "ll_cache_destroy", "ll_attend_chunk", "ll_recache",
+           "ll_recache_attend", "ll_reset", "ll_cache_state", "ll_cache_read", "ll_sync",
+           "ll_cache_info", "ll_frame_slot", "ll_resident_frames", "ll_launch_count",
+           "ll_debug_inject_stall", "ll_debug_use_simt", "ll_profile_enable", "ll_profile_read")
+LL_KERNEL_ATTEND, LL_KERNEL_PREFILL, LL_KERNEL_COPY = 0, 1, 2
+
+
+class LLError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s" % (where, STATUS[status] if 0 <= status < len(STATUS) else status))
+
+
+_lib_handle = None
+
+
+def _lib() -> ctypes.CDLL:
+    """Load libll.so (built in-tree); fail loudly when it is missing."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libll.so is not built: run `python -m windowed_sink_attention_ll_b300.build_lib`"
+                               " (or __graft_entry__.build())")
+        lib = ctypes.CDLL(LIB_PATH)
+        vp, i32, i64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
+        sig = {
+            "ll_status_str": (ctypes.c_char_p, [i32]),
+            "ll_cache_create": (i32, [ctypes.POINTER(vp), i32, i32, i32, i32, i32, i32, i32, i32]),
+            "ll_cache_destroy": (None, [vp]),
+            "ll_attend_chunk": (i32, [vp, i32, vp, vp, vp, vp, i32, vp]),
+            "ll_recache": (i32, [vp, i32, vp, vp, vp]),
+            "ll_recache_attend": (i32, [vp, i32, vp, vp, vp, vp, vp]),
+            "ll_reset": (i32, [vp]),
+            "ll_cache_state": (i32, [vp, i32, ctypes.POINTER(i64), ctypes.POINTER(i64)]),
+            "ll_cache_read": (i32, [vp, i32, vp, vp]),
+            "ll_sync": (i32, [vp]),
+            "ll_cache_info": (i32, [vp, ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_size_t),
+                                    ctypes.POINTER(i32)]),
+            "ll_frame_slot": (i32, [i32, i32, i64]),
+            "ll_resident_frames": (i32, [i32, i32, i64, ctypes.POINTER(i64)]),
+            "ll_launch_count": (ctypes.c_uint64, []),
+            "ll_debug_inject_stall": (i32, [vp, i32, i32]),
+            "ll_debug_use_simt": (i32, [vp, i32]),
+            "ll_profile_enable": (i32, [vp, i32]),
+            "ll_profile_read": (i32, [vp, i32, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(lib, name)
+            f.restype = res
+            f.argtypes = args
+        _lib_handle = lib
+    return _lib_handle
+
+
+def _check(status: int, where: str) -> None:
+    if status != LL_OK:
+        raise LLError(status, where)
+
+
+class LLCache:
+    """Handle of one ll_cache plus its shape (for argument checks)."""
+
+    def __init__(self, ptr, layers, heads, head_dim, tokens_per_frame, sink_frames, window_frames,
+                 chunk_frames, dtype):
+        self.ptr = ptr
+        self.layers, self.heads, self.head_dim = layers, heads, head_dim
+        self.T, self.S, self.W, self.C = tokens_per_frame, sink_frames, window_frames, chunk_frames
+        self.dtype = dtype
+        self.torch_dtype = torch.bfloat16 if dtype == LL_BF16 else torch.float32
+        self.device = torch.cuda.current_device() if torch.cuda.is_available() else None
+
+    @property
+    def slots(self) -> int:
+        return self.S + self.W
+
+    def close(self) -> None:
+        if self.ptr:
+            _lib().ll_cache_destroy(self.ptr)
+            self.ptr = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # convenience methods (same calls as the module functions)
+    def attend_chunk(self, layer, q, k, v, out, commit, stream=None):
+        return ll_attend_chunk(self, layer, q, k, v, out, commit, stream)
+
+    def recache(self, layer, k_win, v_win, stream=None):
+        return ll_recache(self, layer, k_win, v_win, stream)
+
+    def recache_attend(self, layer, q_win, k_win, v_win, out_win, stream=None):
+        return ll_recache_attend(self, layer, q_win, k_win, v_win, out_win, stream)
+
+    def reset(self):
+        return ll_reset(self)
+
+    def state(self, layer):
+        return ll_cache_state(self, layer)
+
+    def read(self, layer):
+        return ll_cache_read(self, layer)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(cache: LLCache, t, tokens: int, name: str) -> int:
+    """Device pointer of a [tokens, H, d] tensor in the cache dtype."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if t.dtype != cache.torch_dtype:
+        raise ValueError("%s has dtype %s, the cache holds %s" % (name, t.dtype, cache.torch_dtype))
+    if tuple(t.shape) != (tokens, cache.heads, cache.head_dim):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape),
+                                                          (tokens, cache.heads, cache.head_dim)))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    return t.data_ptr()
+
+
+def ll_status_str(status: int) -> str:
+    return _lib().ll_status_str(status).decode()
+
+
+def ll_cache_create(layers, heads, head_dim, tokens_per_frame, sink_frames, window_frames, chunk_frames,
+                    dtype=LL_BF16) -> LLCache:
+    if isinstance(dtype, torch.dtype):
+        dtype = LL_BF16 if dtype == torch.bfloat16 else LL_FP32 if dtype == torch.float32 else -1
+    out = ctypes.c_void_p()
+    _check(_lib().ll_cache_create(ctypes.byref(out), layers, heads, head_dim, tokens_per_frame, sink_frames,
+                                  window_frames, chunk_frames, dtype), "ll_cache_create")
+    return LLCache(out.value, layers, heads, head_dim, tokens_per_frame, sink_frames, window_frames,
+                   chunk_frames, dtype)
+
+
+def ll_cache_destroy(cache: LLCache) -> None:
+    cache.close()
+
+
+def ll_attend_chunk(cache: LLCache, layer: int, q, k, v, out, commit: bool, stream=None) -> None:
+    L = cache.C * cache.T
+    args = [_ptr(cache, t, L, n) for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out"))]
+    _check(_lib().ll_attend_chunk(cache.ptr, layer, *args, 1 if commit else 0, _stream(stream)),
+           "ll_attend_chunk")
+
+
+def ll_recache(cache: LLCache, layer: int, k_win, v_win, stream=None) -> None:
+    L = k_win.shape[0] if isinstance(k_win, torch.Tensor) else -1
+    _check(_lib().ll_recache(cache.ptr, layer, _ptr(cache, k_win, L, "k_win"), _ptr(cache, v_win, L, "v_win"),
+                             _stream(stream)), "ll_recache")
+
+
+def ll_recache_attend(cache: LLCache, layer: int, q_win, k_win, v_win, out_win, stream=None) -> None:
+    L = q_win.shape[0] if isinstance(q_win, torch.Tensor) else -1
+    ptrs = [_ptr(cache, t, L, n) for t, n in ((q_win, "q_win"), (k_win, "k_win"), (v_win, "v_win"),
+                                              (out_win, "out_win"))]
+    _check(_lib().ll_recache_attend(cache.ptr, layer, *ptrs, _stream(stream)), "ll_recache_attend")
+
+
+def ll_reset(cache: LLCache) -> None:
+    _check(_lib().ll_reset(cache.ptr), "ll_reset")
+
+
+def ll_cache_state(cache: LLCache, layer: int):
+    """(frames committed, frame_of_slot list); synchronises the device."""
+    n = ctypes.c_int64()
+    table = (ctypes.c_int64 * max(1, cache.slots))()
+    _check(_lib().ll_cache_state(cache.ptr, layer, ctypes.byref(n), table), "ll_cache_state")
+    return n.value, [table[i] for i in range(cache.slots)]
+
+
+def ll_cache_read(cache: LLCache, layer: int):
+    """Raw K and V of one layer as CPU tensors [H, S+W, T, d] (synchronises)."""
+    shape = (cache.heads, cache.slots, cache.T, cache.head_dim)
+    hk = torch.empty(shape, dtype=cache.torch_dtype)
+    hv = torch.empty(shape, dtype=cache.torch_dtype)
+    _check(_lib().ll_cache_read(cache.ptr, layer, hk.data_ptr(), hv.data_ptr()), "ll_cache_read")
+    return hk, hv
+
+
+def ll_sync(cache: LLCache) -> None:
+    _check(_lib().ll_sync(cache.ptr), "ll_sync")
+
+
+def ll_cache_info(cache: LLCache):
+    slots, eb = ctypes.c_int(), ctypes.c_int()
+    nbytes = ctypes.c_size_t()
+    _check(_lib().ll_cache_info(cache.ptr, ctypes.byref(slots), ctypes.byref(nbytes), ctypes.byref(eb)),
+           "ll_cache_info")
+    return slots.value, nbytes.value, eb.value
+
+
+def ll_frame_slot(sink_frames: int, window_frames: int, f: int) -> int:
+    return _lib().ll_frame_slot(sink_frames, window_frames, f)
+
+
+def ll_resident_frames(sink_frames: int, window_frames: int, n: int) -> list:
+    buf = (ctypes.c_int64 * max(1, sink_frames + window_frames))()
+    cnt = _lib().ll_resident_frames(sink_frames, window_frames, n, buf)
+    return [buf[i] for i in range(cnt)]
+
+
+def ll_resident_count(sink_frames: int, window_frames: int, n: int) -> int:
+    return len(ll_resident_frames(sink_frames, window_frames, n))
+
+
+def ll_launch_count() -> int:
+    return _lib().ll_launch_count()
+
+
+def ll_debug_inject_stall(cache: LLCache, enable: bool, timeout_us: int) -> None:
+    _check(_lib().ll_debug_inject_stall(cache.ptr, 1 if enable else 0, timeout_us), "ll_debug_inject_stall")
+
+
+def ll_debug_use_simt(cache: LLCache, enable: bool) -> None:
+    _check(_lib().ll_debug_use_simt(cache.ptr, 1 if enable else 0), "ll_debug_use_simt")
+
+
+def ll_profile_enable(cache: LLCache, enable: bool) -> None:
+    _check(_lib().ll_profile_enable(cache.ptr, 1 if enable else 0), "ll_profile_enable")
+
+
+def ll_profile_read(cache: LLCache, kind: int):
+    """(launches, summed device milliseconds) of one kernel kind; synchronises."""
+    n = ctypes.c_int64()
+    ms = ctypes.c_double()
+    _check(_lib().ll_profile_read(cache.ptr, kind, ctypes.byref(n), ctypes.byref(ms)), "ll_profile_read")
+    return n.value, ms.value

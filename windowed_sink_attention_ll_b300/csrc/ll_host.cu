@@ -1,0 +1,466 @@
+// Host side of libll: the cache object, argument and state checks, the
+// frame-to-slot bookkeeping, and the C ABI declared in include/ll.h.
+//
+// Cache rule ("LongLive: Real-time Interactive Long Video Generation", §3.3
+// Efficient Long Inference, "Frame sink" and "Short window attention"): the
+// first S frames of a layer are a sink that is never evicted; the next frames
+// roll through a window of W slots, frame f >= S living in slot
+// S + ((f - S) mod W).  After n commits the resident frames are
+// 0..min(S,n)-1 and max(S, n-W)..n-1, and their slots always form the prefix
+// [0, R) of the slot range, so the attention kernels read the resident keys as
+// one contiguous run of R*T rows per head.
+#include <atomic>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "ll.h"
+#include "ll_internal.h"
+
+namespace ll {
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+}  // namespace ll
+
+struct ll_cache {
+  int L, H, D, T, S, W, C;
+  ll_dtype dtype;
+  int eb;                 // element bytes
+  int device;
+  size_t layer_elems;     // elements of one layer's K (= V)
+  void* k = nullptr;      // [L][H][S+W][T][D]
+  void* v = nullptr;
+  std::vector<int64_t> n;               // frames committed per layer
+  std::vector<int64_t> fos;             // frame_of_slot, L x (S+W)
+  unsigned* err_host = nullptr;         // mapped host word written by kernels
+  unsigned* err_dev = nullptr;
+  int stall_inject = 0;
+  int stall_timeout_us = 0;
+  int use_simt = 0;
+  // per-kernel timing (ll_profile_enable / ll_profile_read)
+  struct Mark {
+    int kind;
+    cudaEvent_t start, stop;
+  };
+  bool profiling = false;
+  std::vector<Mark> marks;
+  std::vector<cudaEvent_t> event_pool;
+};
+
+namespace {
+
+constexpr long long kDefaultTimeoutNs = 2000000000LL;  // 2 s: no legal wait comes near it
+
+int64_t resident_count(int S, int W, int64_t n) {
+  const int64_t sink = n < S ? n : S;
+  int64_t win = n - S;
+  if (win < 0) win = 0;
+  if (win > W) win = W;
+  return sink + win;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+ll_status take_device_error(ll_cache* c) {
+  volatile unsigned* e = c->err_host;
+  const unsigned v = *e;
+  if (v != 0) {
+    *e = 0;
+    return LL_ERR_DEVICE_TIMEOUT;
+  }
+  return LL_OK;
+}
+
+ll_status set_device(const ll_cache* c) {
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return LL_ERR_CUDA;
+  if (cur != c->device && cudaSetDevice(c->device) != cudaSuccess) return LL_ERR_CUDA;
+  return LL_OK;
+}
+
+ll::AttendArgs base_args(ll_cache* c, int layer) {
+  ll::AttendArgs a;
+  std::memset(&a, 0, sizeof(a));
+  const size_t off = c->layer_elems * (size_t)layer * (size_t)c->eb;
+  a.kc = static_cast<const char*>(c->k) + off;
+  a.vc = static_cast<const char*>(c->v) + off;
+  a.cache_head_elems = (int64_t)(c->S + c->W) * c->T * c->D;
+  a.heads = c->H;
+  a.head_dim = c->D;
+  a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)c->D));
+  a.err = c->err_dev;
+  a.stall_inject = c->stall_inject;
+  a.timeout_ns = c->stall_inject ? (long long)c->stall_timeout_us * 1000LL : kDefaultTimeoutNs;
+  c->stall_inject = 0;  // one launch only
+  return a;
+}
+
+cudaEvent_t pooled_event(ll_cache* c) {
+  if (!c->event_pool.empty()) {
+    cudaEvent_t e = c->event_pool.back();
+    c->event_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+// Brackets one launch with events when profiling is on.
+struct ProfileScope {
+  ll_cache* c;
+  cudaStream_t st;
+  int kind;
+  cudaEvent_t start = nullptr;
+  ProfileScope(ll_cache* c_, cudaStream_t st_, int kind_) : c(c_), st(st_), kind(kind_) {
+    if (c->profiling && (start = pooled_event(c)) != nullptr) cudaEventRecord(start, st);
+  }
+  void done() {
+    if (!start) return;
+    cudaEvent_t stop = pooled_event(c);
+    if (!stop) return;
+    cudaEventRecord(stop, st);
+    c->marks.push_back({kind, start, stop});
+  }
+};
+
+ll_status launch_attend(ll_cache* c, const ll::AttendArgs& a, cudaStream_t st) {
+  ProfileScope prof(c, st, a.mode == 1 ? LL_KERNEL_PREFILL : LL_KERNEL_ATTEND);
+  cudaError_t e;
+  if (c->dtype == LL_FP32 || c->use_simt) {
+    e = ll::launch_attend_simt(a, c->eb, st);
+  } else {
+    e = ll::launch_attend_bf16_tc(a, st);
+  }
+  prof.done();
+  return e == cudaSuccess ? LL_OK : LL_ERR_CUDA;
+}
+
+ll_status launch_copy(ll_cache* c, int layer, const void* k, const void* v, const std::vector<int>& slot_of,
+                      cudaStream_t st) {
+  ll::CopyFramesArgs a;
+  std::memset(&a, 0, sizeof(a));
+  const size_t off = c->layer_elems * (size_t)layer * (size_t)c->eb;
+  a.src_k = k;
+  a.src_v = v;
+  a.dst_k = static_cast<char*>(c->k) + off;
+  a.dst_v = static_cast<char*>(c->v) + off;
+  a.frames = (int)slot_of.size();
+  a.tokens_per_frame = c->T;
+  a.heads = c->H;
+  a.head_dim = c->D;
+  a.slots = c->S + c->W;
+  a.elem_bytes = c->eb;
+  for (size_t i = 0; i < slot_of.size(); ++i) a.slot_of[i] = slot_of[i];
+  ProfileScope prof(c, st, LL_KERNEL_COPY);
+  const cudaError_t e = ll::launch_copy_frames(a, st);
+  prof.done();
+  return e == cudaSuccess ? LL_OK : LL_ERR_CUDA;
+}
+
+ll_status check_layer(const ll_cache* c, int layer) {
+  if (!c) return LL_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= c->L) return LL_ERR_INVALID_ARG;
+  return LL_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ll_status_str(ll_status s) {
+  switch (s) {
+    case LL_OK: return "LL_OK";
+    case LL_ERR_INVALID_ARG: return "LL_ERR_INVALID_ARG";
+    case LL_ERR_UNSUPPORTED: return "LL_ERR_UNSUPPORTED";
+    case LL_ERR_OOM: return "LL_ERR_OOM";
+    case LL_ERR_STATE: return "LL_ERR_STATE";
+    case LL_ERR_CUDA: return "LL_ERR_CUDA";
+    case LL_ERR_DEVICE_TIMEOUT: return "LL_ERR_DEVICE_TIMEOUT";
+  }
+  return "LL_ERR_UNKNOWN";
+}
+
+int ll_frame_slot(int S, int W, int64_t f) {
+  if (f < 0) return -1;
+  if (f < S) return (int)f;
+  if (W <= 0) return -1;
+  return S + (int)((f - S) % W);
+}
+
+int ll_resident_frames(int S, int W, int64_t n, int64_t* frames) {
+  int cnt = 0;
+  const int64_t sink = n < S ? n : S;
+  for (int64_t f = 0; f < sink; ++f) frames[cnt++] = f;
+  int64_t lo = n - W;
+  if (lo < S) lo = S;
+  for (int64_t f = lo; f < n; ++f) frames[cnt++] = f;
+  return cnt;
+}
+
+uint64_t ll_launch_count(void) { return ll::g_launches.load(std::memory_order_relaxed); }
+
+ll_status ll_cache_create(ll_cache** out, int layers, int heads, int head_dim, int tokens_per_frame,
+                          int sink_frames, int window_frames, int chunk_frames, ll_dtype dtype) {
+  if (!out) return LL_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (layers < 1 || heads < 1 || tokens_per_frame < 1 || chunk_frames < 1 || sink_frames < 0 ||
+      window_frames < 0)
+    return LL_ERR_INVALID_ARG;
+  if (dtype != LL_BF16 && dtype != LL_FP32) return LL_ERR_INVALID_ARG;
+  if (head_dim != 64 && head_dim != 128) return LL_ERR_UNSUPPORTED;
+  const int slots = sink_frames + window_frames;
+  if (slots > ll::kMaxFrameTable || chunk_frames > ll::kMaxFrameTable) return LL_ERR_UNSUPPORTED;
+  // kernel grids: (frames x heads) copy blocks; 32-bit token counts per call
+  if ((int64_t)ll::kMaxFrameTable * heads > 65535) return LL_ERR_UNSUPPORTED;
+  if ((int64_t)(slots + chunk_frames) * tokens_per_frame > (1LL << 30)) return LL_ERR_UNSUPPORTED;
+
+  ll_cache* c = new ll_cache();
+  c->L = layers;
+  c->H = heads;
+  c->D = head_dim;
+  c->T = tokens_per_frame;
+  c->S = sink_frames;
+  c->W = window_frames;
+  c->C = chunk_frames;
+  c->dtype = dtype;
+  c->eb = dtype == LL_BF16 ? 2 : 4;
+  c->layer_elems = (size_t)heads * slots * tokens_per_frame * head_dim;
+  c->n.assign(layers, 0);
+  c->fos.assign((size_t)layers * slots, -1);
+  if (cudaGetDevice(&c->device) != cudaSuccess) {
+    delete c;
+    return LL_ERR_CUDA;
+  }
+  // at least one 256-byte block, so a cache without slots (S = W = 0) still
+  // hands the kernels a valid base address
+  size_t bytes = c->layer_elems * layers * c->eb;
+  if (bytes < 256) bytes = 256;
+  {
+    if (cudaMalloc(&c->k, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      delete c;
+      return LL_ERR_OOM;
+    }
+    if (cudaMalloc(&c->v, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(c->k);
+      delete c;
+      return LL_ERR_OOM;
+    }
+    if (cudaMemset(c->k, 0, bytes) != cudaSuccess || cudaMemset(c->v, 0, bytes) != cudaSuccess) {
+      cudaFree(c->k);
+      cudaFree(c->v);
+      delete c;
+      return LL_ERR_CUDA;
+    }
+  }
+  if (cudaHostAlloc(reinterpret_cast<void**>(&c->err_host), 256, cudaHostAllocMapped) != cudaSuccess ||
+      cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->err_dev), c->err_host, 0) != cudaSuccess) {
+    cudaGetLastError();
+    if (c->err_host) cudaFreeHost(c->err_host);
+    cudaFree(c->k);
+    cudaFree(c->v);
+    delete c;
+    return LL_ERR_CUDA;
+  }
+  *c->err_host = 0;
+  *out = c;
+  return LL_OK;
+}
+
+void ll_cache_destroy(ll_cache* c) {
+  if (!c) return;
+  set_device(c);
+  cudaDeviceSynchronize();
+  for (auto& m : c->marks) {
+    cudaEventDestroy(m.start);
+    cudaEventDestroy(m.stop);
+  }
+  for (auto e : c->event_pool) cudaEventDestroy(e);
+  cudaFree(c->k);
+  cudaFree(c->v);
+  cudaFreeHost(c->err_host);
+  delete c;
+}
+
+ll_status ll_attend_chunk(ll_cache* c, int layer, const void* q, const void* k, const void* v, void* out,
+                          int commit, void* stream) {
+  if (ll_status s = check_layer(c, layer)) return s;
+  if (!q || !k || !v || !out) return LL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return LL_ERR_INVALID_ARG;
+  if (out == q || out == k || out == v) return LL_ERR_INVALID_ARG;
+  if (ll_status s = take_device_error(c)) return s;
+  if (ll_status s = set_device(c)) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t t0 = c->n[layer];
+  const int64_t R = resident_count(c->S, c->W, t0);
+  ll::AttendArgs a = base_args(c, layer);
+  a.q = q;
+  a.out = out;
+  a.La = (int)(R * c->T);
+  a.kn = k;
+  a.vn = v;
+  a.Lb = c->C * c->T;
+  a.Lq = c->C * c->T;
+  a.mode = 0;
+  a.block_tokens = c->C * c->T;
+  if (ll_status s = launch_attend(c, a, st)) return s;
+  if (!commit) return LL_OK;
+
+  // Commit: frames t0 .. t0+C-1.  A frame that the same commit would already
+  // evict (W < C) is not written, so the copy has no write-write conflicts.
+  const int64_t n1 = t0 + c->C;
+  int64_t win_lo = n1 - c->W;
+  if (win_lo < c->S) win_lo = c->S;
+  std::vector<int> slot_of(c->C, -1);
+  for (int i = 0; i < c->C; ++i) {
+    const int64_t f = t0 + i;
+    if (f < c->S || f >= win_lo) slot_of[i] = ll_frame_slot(c->S, c->W, f);
+  }
+  if (ll_status s = launch_copy(c, layer, k, v, slot_of, st)) return s;
+  int64_t* fos = &c->fos[(size_t)layer * (c->S + c->W)];
+  for (int i = 0; i < c->C; ++i)
+    if (slot_of[i] >= 0) fos[slot_of[i]] = t0 + i;
+  c->n[layer] = n1;
+  return LL_OK;
+}
+
+static ll_status recache_common(ll_cache* c, int layer, const void* q_win, const void* k_win,
+                                const void* v_win, void* out_win, void* stream) {
+  if (ll_status s = check_layer(c, layer)) return s;
+  if (!k_win || !v_win) return LL_ERR_INVALID_ARG;
+  if (!aligned16(k_win) || !aligned16(v_win)) return LL_ERR_INVALID_ARG;
+  if (q_win && (!out_win || !aligned16(q_win) || !aligned16(out_win))) return LL_ERR_INVALID_ARG;
+  if (q_win && (out_win == q_win || out_win == k_win || out_win == v_win)) return LL_ERR_INVALID_ARG;
+  const int64_t n = c->n[layer];
+  std::vector<int64_t> frames(c->S + c->W + 1);
+  const int R = ll_resident_frames(c->S, c->W, n, frames.data());
+  if (R == 0) return LL_ERR_STATE;
+  if (ll_status s = take_device_error(c)) return s;
+  if (ll_status s = set_device(c)) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (q_win) {
+    ll::AttendArgs a = base_args(c, layer);
+    a.q = q_win;
+    a.out = out_win;
+    a.La = 0;
+    a.kn = k_win;
+    a.vn = v_win;
+    a.Lb = R * c->T;
+    a.Lq = R * c->T;
+    a.mode = 1;
+    a.block_tokens = c->C * c->T;
+    if (ll_status s = launch_attend(c, a, st)) return s;
+  }
+  std::vector<int> slot_of(R);
+  for (int i = 0; i < R; ++i) slot_of[i] = ll_frame_slot(c->S, c->W, frames[i]);
+  return launch_copy(c, layer, k_win, v_win, slot_of, st);
+}
+
+ll_status ll_recache(ll_cache* c, int layer, const void* k_win, const void* v_win, void* stream) {
+  return recache_common(c, layer, nullptr, k_win, v_win, nullptr, stream);
+}
+
+ll_status ll_recache_attend(ll_cache* c, int layer, const void* q_win, const void* k_win, const void* v_win,
+                            void* out_win, void* stream) {
+  if (!q_win || !out_win) return LL_ERR_INVALID_ARG;
+  return recache_common(c, layer, q_win, k_win, v_win, out_win, stream);
+}
+
+ll_status ll_reset(ll_cache* c) {
+  if (!c) return LL_ERR_INVALID_ARG;
+  std::fill(c->n.begin(), c->n.end(), 0);
+  std::fill(c->fos.begin(), c->fos.end(), -1);
+  return LL_OK;
+}
+
+ll_status ll_sync(ll_cache* c) {
+  if (!c) return LL_ERR_INVALID_ARG;
+  if (ll_status s = set_device(c)) return s;
+  if (cudaDeviceSynchronize() != cudaSuccess) return LL_ERR_CUDA;
+  return take_device_error(c);
+}
+
+ll_status ll_cache_state(ll_cache* c, int layer, int64_t* frames_committed, int64_t* frame_of_slot) {
+  if (ll_status s = check_layer(c, layer)) return s;
+  if (ll_status s = ll_sync(c)) return s;
+  if (frames_committed) *frames_committed = c->n[layer];
+  if (frame_of_slot) {
+    const int slots = c->S + c->W;
+    for (int i = 0; i < slots; ++i) frame_of_slot[i] = c->fos[(size_t)layer * slots + i];
+  }
+  return LL_OK;
+}
+
+ll_status ll_cache_read(ll_cache* c, int layer, void* host_k, void* host_v) {
+  if (ll_status s = check_layer(c, layer)) return s;
+  if (!host_k || !host_v) return LL_ERR_INVALID_ARG;
+  if (ll_status s = ll_sync(c)) return s;
+  const size_t bytes = c->layer_elems * c->eb;
+  const size_t off = bytes * (size_t)layer;
+  if (bytes == 0) return LL_OK;
+  if (cudaMemcpy(host_k, static_cast<char*>(c->k) + off, bytes, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(host_v, static_cast<char*>(c->v) + off, bytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return LL_ERR_CUDA;
+  return LL_OK;
+}
+
+ll_status ll_cache_info(const ll_cache* c, int* slots, size_t* layer_bytes, int* elem_bytes) {
+  if (!c) return LL_ERR_INVALID_ARG;
+  if (slots) *slots = c->S + c->W;
+  if (layer_bytes) *layer_bytes = c->layer_elems * c->eb;
+  if (elem_bytes) *elem_bytes = c->eb;
+  return LL_OK;
+}
+
+ll_status ll_debug_inject_stall(ll_cache* c, int enable, int timeout_us) {
+  if (!c || timeout_us < 0) return LL_ERR_INVALID_ARG;
+  c->stall_inject = enable ? 1 : 0;
+  c->stall_timeout_us = timeout_us;
+  return LL_OK;
+}
+
+ll_status ll_profile_enable(ll_cache* c, int enable) {
+  if (!c) return LL_ERR_INVALID_ARG;
+  c->profiling = enable != 0;
+  return LL_OK;
+}
+
+ll_status ll_profile_read(ll_cache* c, int kind, int64_t* launches, double* total_ms) {
+  if (!c || kind < 0 || kind >= LL_KERNEL_KINDS) return LL_ERR_INVALID_ARG;
+  if (ll_status s = ll_sync(c)) return s;
+  int64_t n = 0;
+  double ms = 0.0;
+  std::vector<ll_cache::Mark> keep;
+  for (auto& m : c->marks) {
+    if (m.kind != kind) {
+      keep.push_back(m);
+      continue;
+    }
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, m.start, m.stop) == cudaSuccess) {
+      ms += t;
+      ++n;
+    }
+    c->event_pool.push_back(m.start);
+    c->event_pool.push_back(m.stop);
+  }
+  c->marks.swap(keep);
+  if (launches) *launches = n;
+  if (total_ms) *total_ms = ms;
+  return LL_OK;
+}
+
+ll_status ll_debug_use_simt(ll_cache* c, int enable) {
+  if (!c) return LL_ERR_INVALID_ARG;
+  c->use_simt = enable ? 1 : 0;
+  return LL_OK;
+}
+
+}  // extern "C"

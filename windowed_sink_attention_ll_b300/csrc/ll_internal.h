@@ -1,0 +1,72 @@
+// Internal declarations shared by the host layer and the kernels of libll.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ll {
+
+// Largest number of frames one copy launch may place (C for a commit, S + W for a recache).
+constexpr int kMaxFrameTable = 512;
+
+// Device error word codes (OR-ed together by kernels, read and cleared by the host).
+constexpr unsigned kErrTimeout = 1u;
+
+// ---------------------------------------------------------------------------
+// Frame copy: chunk/recache K,V [frames*T][H][d] (token-major) -> cache slots
+// [H][slots*T][d] (head-major).  slot_of[i] is the destination slot of source
+// frame i, or -1 to skip it.
+// ---------------------------------------------------------------------------
+struct CopyFramesArgs {
+  const void* src_k;
+  const void* src_v;
+  void* dst_k;  // this layer's K cache: head 0, slot 0
+  void* dst_v;
+  int frames;
+  int tokens_per_frame;
+  int heads;
+  int head_dim;
+  int slots;       // S + W
+  int elem_bytes;  // 2 or 4
+  int slot_of[kMaxFrameTable];
+};
+
+cudaError_t launch_copy_frames(const CopyFramesArgs& a, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// Attention over two key/value sources:
+//   source A: rows [0, La) of this layer's head-major cache (the resident slots,
+//             which always form a prefix of the slots);
+//   source B: rows [0, Lb) of a caller tensor [Lb][H][d] (the chunk's own K/V,
+//             or the recache window in prefill mode).
+// mode 0 (attend): every query sees all La + Lb keys.
+// mode 1 (prefill): La = 0 and query row i sees keys j of source B with
+//             j / block_tokens <= i / block_tokens.
+// ---------------------------------------------------------------------------
+struct AttendArgs {
+  const void* q;      // [Lq][H][d]
+  void* out;          // [Lq][H][d]
+  const void* kc;     // cache K of this layer (head 0, slot 0)
+  const void* vc;
+  int64_t cache_head_elems;  // elements between consecutive heads in the cache
+  int La;
+  const void* kn;     // [Lb][H][d]
+  const void* vn;
+  int Lb;
+  int Lq;
+  int heads;
+  int head_dim;
+  int mode;
+  int block_tokens;
+  float scale_log2;   // log2(e) / sqrt(d)
+  unsigned* err;      // device-visible error word
+  int stall_inject;   // test hook: skip one barrier arrival
+  long long timeout_ns;
+};
+
+cudaError_t launch_attend_bf16_tc(const AttendArgs& a, cudaStream_t stream);
+cudaError_t launch_attend_simt(const AttendArgs& a, int elem_bytes, cudaStream_t stream);
+
+void count_launch();
+
+}  // namespace ll
