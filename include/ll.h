@@ -91,7 +91,8 @@ LL_API void ll_cache_destroy(ll_cache* cache);
  * §3.3 "Frame sink" + "Short window attention": per head h,
  *   out_h = softmax(q_h K_h^T / sqrt(d)) V_h,
  *   K/V = [frames 0..min(S,t0)-1 || frames max(S,t0-W)..t0-1 || k/v of this chunk].
- * q, k, v, out: [C*T][H][d] device buffers (out may not alias q, k or v).
+ * q, k, v: [C*T][H][d] device buffers in the cache dtype; out: [C*T][H][d] in
+ * the output dtype (see ll_set_output_dtype); out may not alias q, k or v.
  * commit != 0: after the attention, the chunk's K/V are written into the
  * cache: frame f < S into sink slot f, frame f >= S into ring slot
  * S + ((f - S) mod W), replacing the frame W positions older; frames that
@@ -119,6 +120,14 @@ LL_API ll_status ll_recache(ll_cache* cache, int layer, const void* k_win, const
  */
 LL_API ll_status ll_recache_attend(ll_cache* cache, int layer, const void* q_win, const void* k_win,
                             const void* v_win, void* out_win, void* stream);
+
+/*
+ * ll_set_output_dtype -- element type of `out` / `out_win` in later calls.
+ * Default: the cache dtype.  LL_FP32 on a bf16 cache returns the fp32
+ * accumulator result unrounded (bf16 rounding alone costs up to |o| * 2^-9,
+ * which passes 1e-2 once |o| >= 4).  LL_BF16 on an fp32 cache is rejected.
+ */
+LL_API ll_status ll_set_output_dtype(ll_cache* cache, ll_dtype dtype);
 
 /* §4.4 Table 4 ("no KV cache"): drop every frame of every layer (metadata only). */
 LL_API ll_status ll_reset(ll_cache* cache);

@@ -35,7 +35,8 @@ STATUS = ["LL_OK", "LL_ERR_INVALID_ARG", "LL_ERR_UNSUPPORTED", "LL_ERR_OOM", "LL
 EXPORTS = ("ll_status_str", "ll_cache_create", "ll_cache_destroy", "ll_attend_chunk", "ll_recache",
            "ll_recache_attend", "ll_reset", "ll_cache_state", "ll_cache_read", "ll_sync",
            "ll_cache_info", "ll_frame_slot", "ll_resident_frames", "ll_launch_count",
-           "ll_debug_inject_stall", "ll_debug_use_simt", "ll_profile_enable", "ll_profile_read")
+           "ll_debug_inject_stall", "ll_debug_use_simt", "ll_profile_enable", "ll_profile_read",
+           "ll_set_output_dtype")
 LL_KERNEL_ATTEND, LL_KERNEL_PREFILL, LL_KERNEL_COPY = 0, 1, 2
 
 
@@ -76,6 +77,7 @@ def _lib() -> ctypes.CDLL:
             "ll_debug_inject_stall": (i32, [vp, i32, i32]),
             "ll_debug_use_simt": (i32, [vp, i32]),
             "ll_profile_enable": (i32, [vp, i32]),
+            "ll_set_output_dtype": (i32, [vp, i32]),
             "ll_profile_read": (i32, [vp, i32, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]),
         }
         for name, (res, args) in sig.items():
@@ -101,6 +103,7 @@ class LLCache:
         self.T, self.S, self.W, self.C = tokens_per_frame, sink_frames, window_frames, chunk_frames
         self.dtype = dtype
         self.torch_dtype = torch.bfloat16 if dtype == LL_BF16 else torch.float32
+        self.out_dtype = self.torch_dtype
         self.device = torch.cuda.current_device() if torch.cuda.is_available() else None
 
     @property
@@ -147,13 +150,14 @@ def _stream(stream) -> int:
 
 
 def _ptr(cache: LLCache, t, tokens: int, name: str) -> int:
-    """Device pointer of a [tokens, H, d] tensor in the cache dtype."""
+    """Device pointer of a [tokens, H, d] tensor in the cache dtype (outputs: the output dtype)."""
     if not isinstance(t, torch.Tensor):
         raise TypeError("%s must be a torch.Tensor" % name)
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
-    if t.dtype != cache.torch_dtype:
-        raise ValueError("%s has dtype %s, the cache holds %s" % (name, t.dtype, cache.torch_dtype))
+    want = cache.out_dtype if name.startswith("out") else cache.torch_dtype
+    if t.dtype != want:
+        raise ValueError("%s has dtype %s, expected %s" % (name, t.dtype, want))
     if tuple(t.shape) != (tokens, cache.heads, cache.head_dim):
         raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape),
                                                           (tokens, cache.heads, cache.head_dim)))
@@ -270,3 +274,11 @@ def ll_profile_read(cache: LLCache, kind: int):
     ms = ctypes.c_double()
     _check(_lib().ll_profile_read(cache.ptr, kind, ctypes.byref(n), ctypes.byref(ms)), "ll_profile_read")
     return n.value, ms.value
+
+
+def ll_set_output_dtype(cache: LLCache, dtype) -> None:
+    """Element type of later outputs: LL_FP32 / torch.float32, or the cache dtype."""
+    if isinstance(dtype, torch.dtype):
+        dtype = LL_BF16 if dtype == torch.bfloat16 else LL_FP32 if dtype == torch.float32 else -1
+    _check(_lib().ll_set_output_dtype(cache.ptr, dtype), "ll_set_output_dtype")
+    cache.out_dtype = torch.float32 if dtype == LL_FP32 else torch.bfloat16

@@ -82,9 +82,16 @@ __global__ void __launch_bounds__(kWarps * 32) attend_simt_kernel(const __grid_c
   for (int j = 0; j < end; ++j) visit(kn + j * stride, vn + j * stride);
 
   const float inv = l > 0.f ? 1.f / l : 0.f;
-  T* out = static_cast<T*>(a.out) + ((int64_t)row * a.heads + h) * D + lane * E;
+  const int64_t ob = ((int64_t)row * a.heads + h) * D + lane * E;
+  if (a.out_f32) {
+    float* out = static_cast<float*>(a.out) + ob;
 #pragma unroll
-  for (int e = 0; e < E; ++e) out[e] = from_f<T>(o[e] * inv);
+    for (int e = 0; e < E; ++e) out[e] = o[e] * inv;
+  } else {
+    T* out = static_cast<T*>(a.out) + ob;
+#pragma unroll
+    for (int e = 0; e < E; ++e) out[e] = from_f<T>(o[e] * inv);
+  }
 }
 
 template <typename T, int D>

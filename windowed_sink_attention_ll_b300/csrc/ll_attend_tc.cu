@@ -463,14 +463,22 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     if (ok) {
       tc_fence_after();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + ((int64_t)qrow * a.heads + head) * D;
+      const int64_t ob = ((int64_t)qrow * a.heads + head) * D;
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + ob;
+      float* outf = static_cast<float*>(a.out) + ob;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t o[32];
         tmem_ld32(tO + 32 * cc, o);
         tmem_ld_wait();
         reg_fence(o, 32);
-        if (qrow < a.Lq) {
+        if (qrow < a.Lq && a.out_f32) {
+          float4* dst = reinterpret_cast<float4*>(outf + 32 * cc);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(__uint_as_float(o[4 * v + 0]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                 __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+        } else if (qrow < a.Lq) {
           uint4* dst = reinterpret_cast<uint4*>(out + 32 * cc);
 #pragma unroll
           for (int v = 0; v < 4; ++v) {

@@ -42,6 +42,7 @@ struct ll_cache {
   int stall_inject = 0;
   int stall_timeout_us = 0;
   int use_simt = 0;
+  int out_f32 = 0;  // outputs in fp32 on a bf16 cache
   // per-kernel timing (ll_profile_enable / ll_profile_read)
   struct Mark {
     int kind;
@@ -94,6 +95,7 @@ ll::AttendArgs base_args(ll_cache* c, int layer) {
   a.head_dim = c->D;
   a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)c->D));
   a.err = c->err_dev;
+  a.out_f32 = (c->dtype == LL_FP32 || c->out_f32) ? 1 : 0;
   a.stall_inject = c->stall_inject;
   a.timeout_ns = c->stall_inject ? (long long)c->stall_timeout_us * 1000LL : kDefaultTimeoutNs;
   c->stall_inject = 0;  // one launch only
@@ -373,6 +375,18 @@ ll_status ll_recache_attend(ll_cache* c, int layer, const void* q_win, const voi
   return recache_common(c, layer, q_win, k_win, v_win, out_win, stream);
 }
 
+ll_status ll_set_output_dtype(ll_cache* c, ll_dtype dtype) {
+  if (!c) return LL_ERR_INVALID_ARG;
+  if (dtype == LL_FP32) {
+    c->out_f32 = 1;
+  } else if (dtype == LL_BF16 && c->dtype == LL_BF16) {
+    c->out_f32 = 0;
+  } else {
+    return LL_ERR_INVALID_ARG;
+  }
+  return LL_OK;
+}
+
 ll_status ll_reset(ll_cache* c) {
   if (!c) return LL_ERR_INVALID_ARG;
   std::fill(c->n.begin(), c->n.end(), 0);
@@ -400,11 +414,11 @@ ll_status ll_cache_state(ll_cache* c, int layer, int64_t* frames_committed, int6
 
 ll_status ll_cache_read(ll_cache* c, int layer, void* host_k, void* host_v) {
   if (ll_status s = check_layer(c, layer)) return s;
+  const size_t bytes = c->layer_elems * c->eb;
+  if (bytes == 0) return ll_sync(c);  // no slots (S = W = 0): nothing to copy
   if (!host_k || !host_v) return LL_ERR_INVALID_ARG;
   if (ll_status s = ll_sync(c)) return s;
-  const size_t bytes = c->layer_elems * c->eb;
   const size_t off = bytes * (size_t)layer;
-  if (bytes == 0) return LL_OK;
   if (cudaMemcpy(host_k, static_cast<char*>(c->k) + off, bytes, cudaMemcpyDeviceToHost) != cudaSuccess ||
       cudaMemcpy(host_v, static_cast<char*>(c->v) + off, bytes, cudaMemcpyDeviceToHost) != cudaSuccess)
     return LL_ERR_CUDA;

@@ -59,6 +59,7 @@ struct AttendArgs {
   int mode;
   int block_tokens;
   float scale_log2;   // log2(e) / sqrt(d)
+  int out_f32;        // out is fp32 (else the cache dtype)
   unsigned* err;      // device-visible error word
   int stall_inject;   // test hook: skip one barrier arrival
   long long timeout_ns;
