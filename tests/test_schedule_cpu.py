@@ -1,0 +1,76 @@
+"""CPU checks of the tensor-core attend kernel's work schedule, replayed on the host by
+the library itself (ll_debug_attend_schedule runs the same walker the kernel runs)."""
+
+import collections
+
+import pytest
+
+from windowed_sink_attention_ll_b300 import build_lib
+
+SHAPES = [
+    # Lq,   La,    Lb,  heads, max_ctas
+    (4680, 18720, 4680, 12, 148),   # Wan-shaped steady state: 228 items on 148 SMs
+    (4680, 0, 4680, 12, 148),       # first chunk: no cache
+    (4680, 14040, 4680, 12, 148),   # warm-up chunk
+    (48, 144, 48, 2, 148),          # tiny: fewer items than SMs
+    (300, 1200, 300, 2, 148),
+    (4680, 18720, 4680, 12, 7),     # few CTAs: several whole rounds plus a tail
+    (4680, 18720, 4680, 12, 1),     # one CTA does everything
+    (37000, 5000, 37000, 3, 148),   # long items
+    (4680, 37440, 4680, 12, 148),   # longest sweep window (S=3, W=18)
+]
+
+
+@pytest.fixture(scope="module")
+def ll():
+    build_lib.build()
+    import windowed_sink_attention_ll_b300 as mod
+
+    mod._lib()
+    return mod
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=[str(s) for s in SHAPES])
+def test_schedule_covers_every_key_tile_once(ll, shape):
+    Lq, La, Lb, H, max_ctas = shape
+    grid, pieces, splits = ll.ll_debug_attend_schedule(Lq, La, Lb, H, max_ctas)
+    nqb = -(-Lq // 256)
+    items = nqb * H
+    nkv = -(-La // 128) + -(-Lb // 128)
+    assert 1 <= grid <= min(max_ctas, items)
+    seen = collections.Counter()
+    per_cta = collections.Counter()
+    part_slots = {}
+    for cta, item, j0, j1, partial, slot in pieces:
+        assert 0 <= cta < grid and 0 <= item < items and 0 <= j0 < j1 <= nkv
+        for j in range(j0, j1):
+            seen[(item, j)] += 1
+        per_cta[cta] += j1 - j0
+        assert partial == (0 if (j0 == 0 and j1 == nkv) else 1)
+        if partial:
+            assert slot in (2 * cta, 2 * cta + 1)
+            assert slot not in part_slots, "two parts share a scratch slot"
+            part_slots[slot] = item
+    assert len(seen) == items * nkv and set(seen.values()) == {1}
+    # split items and their parts agree with the pieces that wrote partial results
+    split_items = {}
+    for item, slots in splits:
+        assert len(slots) >= 2
+        split_items[item] = sorted(slots)
+    by_item = collections.defaultdict(list)
+    for slot, item in part_slots.items():
+        by_item[item].append(slot)
+    assert {i: sorted(s) for i, s in by_item.items()} == split_items
+    # balance: whole rounds are equal; the tail differs by at most one run boundary
+    if grid == max_ctas and items > grid:
+        lo, hi = min(per_cta.values()), max(per_cta.values())
+        assert hi - lo <= max(1, nkv // 16) + 1, (lo, hi)
+
+
+def test_schedule_splits_only_leftover_items(ll):
+    grid, pieces, splits = ll.ll_debug_attend_schedule(4680, 18720, 4680, 12, 148)
+    assert grid == 148
+    # 228 items: round 0 = items 0..147 whole, items 148..227 shared by all 148 CTAs
+    whole = {p[1] for p in pieces if not p[4]}
+    assert set(range(148)) <= whole
+    assert all(item >= 148 for item, _ in splits)

@@ -36,7 +36,7 @@ EXPORTS = ("ll_status_str", "ll_cache_create", "ll_cache_destroy", "ll_attend_ch
            "ll_recache_attend", "ll_reset", "ll_cache_state", "ll_cache_read", "ll_sync",
            "ll_cache_info", "ll_frame_slot", "ll_resident_frames", "ll_launch_count",
            "ll_debug_inject_stall", "ll_debug_use_simt", "ll_profile_enable", "ll_profile_read",
-           "ll_set_output_dtype")
+           "ll_set_output_dtype", "ll_debug_attend_schedule")
 LL_KERNEL_ATTEND, LL_KERNEL_PREFILL, LL_KERNEL_COPY = 0, 1, 2
 
 
@@ -78,6 +78,9 @@ def _lib() -> ctypes.CDLL:
             "ll_debug_use_simt": (i32, [vp, i32]),
             "ll_profile_enable": (i32, [vp, i32]),
             "ll_set_output_dtype": (i32, [vp, i32]),
+            "ll_debug_attend_schedule": (i32, [i32, i32, i32, i32, i32, ctypes.POINTER(i32),
+                                               ctypes.POINTER(i32), i32, ctypes.POINTER(i32), i32,
+                                               ctypes.POINTER(i32)]),
             "ll_profile_read": (i32, [vp, i32, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]),
         }
         for name, (res, args) in sig.items():
@@ -282,3 +285,26 @@ def ll_set_output_dtype(cache: LLCache, dtype) -> None:
         dtype = LL_BF16 if dtype == torch.bfloat16 else LL_FP32 if dtype == torch.float32 else -1
     _check(_lib().ll_set_output_dtype(cache.ptr, dtype), "ll_set_output_dtype")
     cache.out_dtype = torch.float32 if dtype == LL_FP32 else torch.bfloat16
+
+
+def ll_debug_attend_schedule(Lq: int, La: int, Lb: int, heads: int, max_ctas: int):
+    """Host replay of a tensor-core attend launch's schedule (see include/ll.h).
+
+    Returns (grid, pieces, splits): pieces = list of (cta, item, j0, j1, partial,
+    slot); splits = list of (item, [slots of its parts]).
+    """
+    cap, scap = 6 * 65536, 65536
+    pieces = (ctypes.c_int * cap)()
+    splits = (ctypes.c_int * scap)()
+    grid, nints = ctypes.c_int(), ctypes.c_int()
+    n = _lib().ll_debug_attend_schedule(Lq, La, Lb, heads, max_ctas, ctypes.byref(grid), pieces, cap, splits,
+                                        scap, ctypes.byref(nints))
+    if n < 0:
+        raise LLError(LL_ERR_INVALID_ARG, "ll_debug_attend_schedule")
+    out = [tuple(pieces[6 * i:6 * i + 6]) for i in range(n)]
+    sp, i = [], 0
+    while i < nints.value:
+        cnt = splits[i + 1]
+        sp.append((splits[i], list(splits[i + 2:i + 2 + cnt])))
+        i += 2 + cnt
+    return grid.value, out, sp

@@ -13,9 +13,11 @@
 // (§3.1 "KV recache") there is one source, the recache window, and query row
 // i sees key j iff j / block_tokens <= i / block_tokens.
 //
-// CTA = one head x 256 query rows, split into two 128-row tiles that share
-// every K/V tile.  Warp roles (384 threads):
-//   warp 0      TMA producer: Q once, then K0 V0 K1 V1 ... into a 5-stage ring
+// CTA = one head x 256 query rows (two 128-row tiles that share every K/V
+// tile).  Attend launches are persistent: whole rounds of items, then the
+// left-over items split into runs of key tiles merged by combine_kernel (see
+// "Work schedule").  Warp roles (384 threads):
+//   warp 0      TMA producer: Q per item, then K0 V0 K1 V1 ... into a 5-stage ring
 //   warp 1      TMEM allocator and tcgen05.mma issuer (one thread)
 //   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: thread = row
 //   warps 2-3   idle
@@ -26,10 +28,11 @@
 // one tile overlaps the tensor-core work of the other.  A tcgen05.commit
 // completes only when every earlier MMA of the issuing thread has completed,
 // so when S(j+1) of tile w is ready, PV(j) of tile w is done and the softmax
-// threads may rescale O in place.  O is rescaled only when the running row
-// maximum grows by more than 2^8; the final 1/l uses the same reference
-// maximum, so the result is unchanged.
-//
+// threads may rescale O in place.  The reference max of a row moves only when
+// the running max grows by more than 2^8 (then O and l are rescaled); every
+// P, the row sum l and the final 1/l use that same reference, so the result
+// is unchanged.  The row sum adds the bf16-rounded P that enters P V.
+
 // Every mbarrier wait is bounded (globaltimer).  A wait that runs out sets a
 // CTA-wide abort flag and the device error word; all roles then leave their
 // loops, the producer waits (bounded) for its copies in flight, the MMA
@@ -68,7 +71,29 @@ struct Cfg {
 struct TcParams {
   CUtensorMap tm_q, tm_kc, tm_vc, tm_kn, tm_vn;
   AttendArgs a;
-  int nqb;  // query blocks of NQ * BM rows
+  int nqb;               // query blocks of NQ * BM rows per head
+  int nkv;               // attend: key tiles per item
+  int grid;              // CTAs launched
+  int rounds;            // attend: whole-item rounds
+  int tail_ctas;         // attend: CTAs sharing the left-over items
+  long long tail_iters;  // attend: key tiles of the left-over items
+  float* part;           // scratch: partial O [2*grid][NQ*BM][D], then m and l [2*grid][NQ*BM] each
+};
+
+constexpr int kMaxSplit = 256;  // most CTAs of a persistent attend launch
+
+struct CombineParams {
+  void* out;
+  const float* part;
+  int grid;  // the attend launch's CTAs; scratch slots = 2 * grid
+  int nqb;
+  int Lq;
+  int heads;
+  int out_f32;
+  int nsplit;
+  int item[kMaxSplit];
+  int first[kMaxSplit + 1];  // parts of split k: slot[first[k] .. first[k+1])
+  int slot[2 * kMaxSplit];
 };
 
 // ----------------------------------------------------------------------------
@@ -177,11 +202,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
       : LL_R8(0), LL_R8(8), LL_R8(16), LL_R8(24)
       : "r"(taddr));
 }
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-      LL_W8(0), LL_W8(8), LL_W8(16), LL_W8(24)
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : LL_R8(0), LL_R8(8)
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      LL_W8(0), LL_W8(8)
       : "memory");
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
@@ -216,6 +247,102 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
 }
 
 // ----------------------------------------------------------------------------
+// Work schedule
+// ----------------------------------------------------------------------------
+// Attend mode: an item is (head, 256-row query block); every item has the same
+// nkv key tiles.  The grid is persistent (at most one CTA per SM).  Whole
+// rounds of items come first -- CTA c takes item r*grid + c in round r, so the
+// CTAs sweep the K/V tiles of a few heads in step and each tile is fetched
+// from HBM about once -- and the items left over (fewer than the grid) are cut
+// into equal runs of key tiles across `tail_ctas` CTAs.  A run that covers only
+// part of an item leaves a partial result (unnormalised O, reference max m and
+// sum l per row) in scratch slot 2*c + (0: first run of CTA c, 1: its last
+// run); combine_kernel merges the parts of each split item.
+// Prefill mode: one item per CTA, the longest query blocks first.
+struct Piece {
+  int item;
+  int j0, j1;   // key tiles [j0, j1) of the item
+  int partial;  // 1: write a partial result to scratch slot `slot`
+  int slot;
+};
+
+struct Walker {
+  int r;
+  long long it, end, begin;
+  int single;
+  int done;
+};
+
+__host__ __device__ __forceinline__ void walker_init(Walker& w, const TcParams& p, int cta) {
+  w.r = 0;
+  w.done = 0;
+  w.single = p.a.mode == 1;
+  w.begin = w.end = 0;
+  if (!w.single && cta < p.tail_ctas) {
+    w.begin = (p.tail_iters * cta) / p.tail_ctas;
+    w.end = (p.tail_iters * (cta + 1)) / p.tail_ctas;
+  }
+  w.it = w.begin;
+}
+
+__host__ __device__ __forceinline__ int prefill_nkv(const TcParams& p, int qb) {
+  const AttendArgs& a = p.a;
+  const int qend = (qb + 1) * NQ * BM;
+  const int qlast = (qend < a.Lq ? qend : a.Lq) - 1;
+  const long long e = ((long long)qlast / a.block_tokens + 1) * a.block_tokens;
+  const int kv_end = (int)(e < a.Lb ? e : a.Lb);
+  return (kv_end + BN - 1) / BN;
+}
+
+__host__ __device__ __forceinline__ bool walker_next(Walker& w, const TcParams& p, Piece& pc, int cta) {
+  if (w.single) {
+    if (w.done) return false;
+    w.done = 1;
+    pc.item = cta;
+    pc.j0 = 0;
+    pc.j1 = prefill_nkv(p, p.nqb - 1 - cta / p.a.heads);
+    pc.partial = 0;
+    pc.slot = 0;
+    return true;
+  }
+  if (w.r < p.rounds) {
+    pc.item = w.r * p.grid + cta;
+    pc.j0 = 0;
+    pc.j1 = p.nkv;
+    pc.partial = 0;
+    pc.slot = 0;
+    ++w.r;
+    return true;
+  }
+  if (w.it >= w.end) return false;
+  const long long ti = w.it / p.nkv;
+  const int j0 = (int)(w.it - ti * p.nkv);
+  const long long stop = w.end - ti * p.nkv;
+  const int j1 = (int)(stop < p.nkv ? stop : p.nkv);
+  pc.item = p.rounds * p.grid + (int)ti;
+  pc.j0 = j0;
+  pc.j1 = j1;
+  pc.partial = !(j0 == 0 && j1 == p.nkv);
+  pc.slot = 2 * cta + (w.it == w.begin ? 0 : 1);
+  w.it = ti * p.nkv + j1;
+  return true;
+}
+
+// head, first query row and cache-tile count of an item
+__device__ __forceinline__ void item_geom(const TcParams& p, int item, int& head, int& q0, int& nA) {
+  if (p.a.mode == 0) {
+    head = item / p.nqb;
+    q0 = (item - head * p.nqb) * NQ * BM;
+    nA = (p.a.La + BN - 1) / BN;
+  } else {
+    const int qb = p.nqb - 1 - item / p.a.heads;
+    head = item - (item / p.a.heads) * p.a.heads;
+    q0 = qb * NQ * BM;
+    nA = 0;
+  }
+}
+
+// ----------------------------------------------------------------------------
 // The kernel
 // ----------------------------------------------------------------------------
 template <int D>
@@ -228,41 +355,27 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
   const uint32_t sQ = base;
   const uint32_t sKV = base + Cf::kSmemKV;
   const uint32_t sBar = base + Cf::kSmemBar;
-  const uint32_t bQ = sBar;
-  const uint32_t bKVfull0 = sBar + 8;
-  const uint32_t bKVempty0 = sBar + 8 * (1 + NS);
-  const uint32_t bS0 = sBar + 8 * (1 + 2 * NS);
-  const uint32_t bP0 = sBar + 8 * (3 + 2 * NS);
-  const uint32_t bO = sBar + 8 * (5 + 2 * NS);
-  const uint32_t bDrain = sBar + 8 * (6 + 2 * NS);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Cf::kSmemBar + 8 * (7 + 2 * NS));
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Cf::kSmemBar + 8 * (7 + 2 * NS) + 4);
+  const uint32_t bQfull = sBar;
+  const uint32_t bQempty = sBar + 8;
+  const uint32_t bKVfull0 = sBar + 16;
+  const uint32_t bKVempty0 = bKVfull0 + 8 * NS;
+  const uint32_t bS0 = bKVempty0 + 8 * NS;
+  const uint32_t bP0 = bS0 + 16;
+  const uint32_t bOfull = bP0 + 16;
+  const uint32_t bOempty = bOfull + 8;
+  const uint32_t bDrain = bOempty + 8;
+  constexpr int kBarBytes = 16 + 16 * NS + 16 + 16 + 24;
+  static_assert(kBarBytes + 8 <= 256, "barrier area");
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Cf::kSmemBar + kBarBytes);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Cf::kSmemBar + kBarBytes + 4);
 
   const AttendArgs& a = p.a;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // Work item: (head, query block).  Prefill schedules the longest rows first.
-  int head, qb;
-  if (a.mode == 0) {
-    head = blockIdx.x / p.nqb;
-    qb = blockIdx.x - head * p.nqb;
-  } else {
-    qb = p.nqb - 1 - (int)(blockIdx.x / a.heads);
-    head = blockIdx.x - (blockIdx.x / a.heads) * a.heads;
-  }
-  const int q0 = qb * NQ * BM;
-  const int nA = (a.La + BN - 1) / BN;
-  int kv_end = a.Lb;
-  if (a.mode == 1) {
-    const int qlast = min(q0 + NQ * BM, a.Lq) - 1;
-    const long long e = ((long long)qlast / a.block_tokens + 1) * a.block_tokens;
-    kv_end = (int)(e < a.Lb ? e : a.Lb);
-  }
-  const int nkv = nA + (kv_end + BN - 1) / BN;
-
   if (threadIdx.x == 0) {
-    mbar_init(bQ, 1);
+    mbar_init(bQfull, 1);
+    mbar_init(bQempty, 1);
     for (int s = 0; s < NS; ++s) {
       mbar_init(bKVfull0 + 8 * s, 1);
       mbar_init(bKVempty0 + 8 * s, 1);
@@ -271,7 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       mbar_init(bS0 + 8 * w, 1);
       mbar_init(bP0 + 8 * w, 128);
     }
-    mbar_init(bO, 1);
+    mbar_init(bOfull, 1);
+    mbar_init(bOempty, NQ * 128);
     mbar_init(bDrain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -288,34 +402,47 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
   const Ctl ctl{abort_flag, a.err, a.timeout_ns};
 
   int tiles_issued = 0;  // producer: K/V tiles whose copies were started
+  int q_issued = 0;      // producer: Q loads started
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------ TMA producer ------------------------------
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_q)) : "memory");
-      mbar_expect_tx(bQ, NQ * Cf::kQBytes);
-      for (int w = 0; w < NQ; ++w)
-        for (int c = 0; c < Cf::kChunks; ++c)
-          tma_load_3d(sQ + (w * Cf::kChunks + c) * kAtom, &p.tm_q, bQ, c * 64, head, q0 + w * BM);
+      Walker wk;
+      walker_init(wk, p, blockIdx.x);
+      Piece pc;
       int u = 0;
-      for (; u < 2 * nkv; ++u) {
-        const int j = u >> 1;
-        const bool is_v = (u & 1) != 0;
-        const int s = u % NS;
-        const int use = u / NS;
-        if (use > 0 && !wait(bKVempty0 + 8 * s, (use - 1) & 1, ctl)) break;
-        const uint32_t full = bKVfull0 + 8 * s;
-        mbar_expect_tx(full, Cf::kTileBytes);
-        const uint32_t dst = sKV + s * Cf::kTileBytes;
-        if (j < nA) {
-          const CUtensorMap* m = is_v ? &p.tm_vc : &p.tm_kc;
-          for (int c = 0; c < Cf::kChunks; ++c) tma_load_3d(dst + c * kAtom, m, full, c * 64, j * BN, head);
-        } else {
-          const CUtensorMap* m = is_v ? &p.tm_vn : &p.tm_kn;
-          for (int c = 0; c < Cf::kChunks; ++c) tma_load_3d(dst + c * kAtom, m, full, c * 64, head, (j - nA) * BN);
+      bool ok = true;
+      while (ok && walker_next(wk, p, pc, blockIdx.x)) {
+        int head, q0, nA;
+        item_geom(p, pc.item, head, q0, nA);
+        // the previous item's Q K^T products must be done with the Q tiles
+        if (q_issued > 0 && !(ok = wait(bQempty, (q_issued - 1) & 1, ctl))) break;
+        mbar_expect_tx(bQfull, NQ * Cf::kQBytes);
+        for (int w = 0; w < NQ; ++w)
+          for (int c = 0; c < Cf::kChunks; ++c)
+            tma_load_3d(sQ + (w * Cf::kChunks + c) * kAtom, &p.tm_q, bQfull, c * 64, head, q0 + w * BM);
+        ++q_issued;
+        for (int j = pc.j0; ok && j < pc.j1; ++j) {
+          for (int is_v = 0; is_v < 2; ++is_v) {
+            const int s = u % NS;
+            const int use = u / NS;
+            if (use > 0 && !(ok = wait(bKVempty0 + 8 * s, (use - 1) & 1, ctl))) break;
+            const uint32_t full = bKVfull0 + 8 * s;
+            mbar_expect_tx(full, Cf::kTileBytes);
+            const uint32_t dst = sKV + s * Cf::kTileBytes;
+            if (j < nA) {
+              const CUtensorMap* m = is_v ? &p.tm_vc : &p.tm_kc;
+              for (int c = 0; c < Cf::kChunks; ++c) tma_load_3d(dst + c * kAtom, m, full, c * 64, j * BN, head);
+            } else {
+              const CUtensorMap* m = is_v ? &p.tm_vn : &p.tm_kn;
+              for (int c = 0; c < Cf::kChunks; ++c)
+                tma_load_3d(dst + c * kAtom, m, full, c * 64, head, (j - nA) * BN);
+            }
+            tiles_issued = ++u;
+          }
         }
       }
-      tiles_issued = u;
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -338,39 +465,54 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
           mma_ts(tmem + 128 * w, tmem + 256 + 128 * w + ks * 8, bd, kIdPV, (acc || ks > 0) ? 1u : 0u);
         }
       };
-      bool ok = wait(bQ, 0, ctl) && wait(bKVfull0, 0, ctl);
-      if (ok) {
+      Walker wk;
+      walker_init(wk, p, blockIdx.x);
+      Piece pc;
+      int u = 0, qi = 0, jt = 0;
+      bool ok = true;
+      while (ok && walker_next(wk, p, pc, blockIdx.x)) {
+        const int n = pc.j1 - pc.j0;
+        if (!(ok = wait(bQfull, qi & 1, ctl))) break;
+        if (!(ok = wait(bKVfull0 + 8 * (u % NS), (u / NS) & 1, ctl))) break;
         tc_fence_after();
-        issue_qk(0, 0);
+        issue_qk(0, u % NS);
         tc_commit(bS0);
-        issue_qk(1, 0);
+        issue_qk(1, u % NS);
         tc_commit(bS0 + 8);
-        tc_commit(bKVempty0);
-        for (int j = 0; j < nkv && ok; ++j) {
-          const int uv = 2 * j + 1, sv = uv % NS;
-          const int uk = 2 * j + 2, sk = uk % NS;
-          const bool more = j + 1 < nkv;
+        tc_commit(bKVempty0 + 8 * (u % NS));
+        if (n == 1) tc_commit(bQempty);
+        for (int t = 0; t < n; ++t) {
+          const int uv = u + 2 * t + 1, sv = uv % NS;
+          const int uk = u + 2 * t + 2, sk = uk % NS;
+          const bool more = t + 1 < n;
           if (!(ok = wait(bKVfull0 + 8 * sv, (uv / NS) & 1, ctl))) break;
-          if (!(ok = wait(bP0, j & 1, ctl))) break;
+          if (!(ok = wait(bP0, (jt + t) & 1, ctl))) break;
+          // the previous item's epilogue must have read O out of tensor memory
+          if (t == 0 && qi > 0 && !(ok = wait(bOempty, (qi - 1) & 1, ctl))) break;
           tc_fence_after();
-          issue_pv(0, sv, j > 0);
+          issue_pv(0, sv, t > 0);
           if (more) {
             if (!(ok = wait(bKVfull0 + 8 * sk, (uk / NS) & 1, ctl))) break;
             tc_fence_after();
             issue_qk(0, sk);
             tc_commit(bS0);
           }
-          if (!(ok = wait(bP0 + 8, j & 1, ctl))) break;
+          if (!(ok = wait(bP0 + 8, (jt + t) & 1, ctl))) break;
           tc_fence_after();
-          issue_pv(1, sv, j > 0);
+          issue_pv(1, sv, t > 0);
           tc_commit(bKVempty0 + 8 * sv);
           if (more) {
             issue_qk(1, sk);
             tc_commit(bS0 + 8);
             tc_commit(bKVempty0 + 8 * sk);
+            if (t + 2 == n) tc_commit(bQempty);
           }
         }
-        if (ok) tc_commit(bO);
+        if (!ok) break;
+        tc_commit(bOfull);
+        u += 2 * n;
+        jt += n;
+        ++qi;
       }
     }
   } else if (warp >= 4) {
@@ -378,119 +520,157 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     const int w = (warp - 4) >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
-    const int qrow = q0 + w * BM + row;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t tS = tmem + lane_off + 256 + 128 * w;
     const uint32_t tO = tmem + lane_off + 128 * w;
     const uint32_t bS = bS0 + 8 * w;
     const uint32_t bP = bP0 + 8 * w;
-    int row_end = a.Lb;
-    if (a.mode == 1) {
-      const long long e = ((long long)qrow / a.block_tokens + 1) * a.block_tokens;
-      row_end = (int)(e < a.Lb ? e : a.Lb);
-    }
     const float sl2 = a.scale_log2;
-    float m = -INFINITY, l = 0.f;
+    Walker wk;
+    walker_init(wk, p, blockIdx.x);
+    Piece pc;
+    int qi = 0, jt = 0;
     bool ok = true;
-    for (int j = 0; j < nkv; ++j) {
-      ok = __all_sync(0xffffffffu, wait(bS, j & 1, ctl));
+    while (ok && walker_next(wk, p, pc, blockIdx.x)) {
+      int head, q0, nA;
+      item_geom(p, pc.item, head, q0, nA);
+      const int qrow = q0 + w * BM + row;
+      int row_end = a.Lb;
+      if (a.mode == 1) {
+        const long long e = ((long long)qrow / a.block_tokens + 1) * a.block_tokens;
+        row_end = (int)(e < a.Lb ? e : a.Lb);
+      }
+      const int n = pc.j1 - pc.j0;
+      float m = -INFINITY, l = 0.f;
+      for (int t = 0; t < n; ++t) {
+        const int j = pc.j0 + t;
+        ok = __all_sync(0xffffffffu, wait(bS, (jt + t) & 1, ctl));
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t r[BN];
+        tmem_ld32(tS + 0, r + 0);
+        tmem_ld32(tS + 32, r + 32);
+        tmem_ld32(tS + 64, r + 64);
+        tmem_ld32(tS + 96, r + 96);
+        tmem_ld_wait();
+        reg_fence(r, BN);
+        const int valid = j < nA ? a.La - j * BN : (a.mode == 1 ? row_end : a.Lb) - (j - nA) * BN;
+        if (valid < BN) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (c >= valid) r[c] = __float_as_uint(-INFINITY);
+        }
+        float mx[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(r[i]);
+#pragma unroll
+        for (int c = 8; c < BN; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(r[c]));
+        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        const float m_new = fmaxf(m, mt * sl2);
+        // the reference max moves (and O is rescaled, after P is written) only
+        // when some row of the warp grew by more than 2^8
+        const bool rescale = t > 0 && __any_sync(0xffffffffu, m_new > m + kRescaleLog2);
+        float alpha = 1.f;
+        if (t == 0 || rescale) {
+          if (rescale && m_new != -INFINITY) alpha = ex2(m - m_new);
+          l *= alpha;
+          m = m_new;
+        }
+        const float mo = (m == -INFINITY) ? 0.f : m;
+        // P = 2^(s*log2e/sqrt(d) - m), rounded to bf16 for the P V product.  The
+        // row sum adds the same rounded values, so numerator and denominator
+        // carry the same rounding and a dominant key keeps its exact weight.
+        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int g = 0; g < BN / 32; ++g) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int c = g * 32 + 2 * i;
+            const float p0 = ex2(fmaf(__uint_as_float(r[c]), sl2, -mo));
+            const float p1 = ex2(fmaf(__uint_as_float(r[c + 1]), sl2, -mo));
+            pk[i] = pack_bf16(p0, p1);
+            ls[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+          }
+          tmem_st16(tS + 16 * g, pk);
+        }
+        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        if (rescale) {
+          // PV of the previous tile has completed (it was issued before this S)
+#pragma unroll 1
+          for (int cc = 0; cc < D / 16; ++cc) {
+            uint32_t o[16];
+            tmem_ld16(tO + 16 * cc, o);
+            tmem_ld_wait();
+            reg_fence(o, 16);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st16(tO + 16 * cc, o);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        if (!(a.stall_inject && jt + t == 0 && w == 0)) mbar_arrive(bP);
+      }
+      if (!ok) break;
+      ok = __all_sync(0xffffffffu, wait(bOfull, qi & 1, ctl));
       if (!ok) break;
       tc_fence_after();
-      uint32_t r[128];
-      tmem_ld32(tS + 0, r + 0);
-      tmem_ld32(tS + 32, r + 32);
-      tmem_ld32(tS + 64, r + 64);
-      tmem_ld32(tS + 96, r + 96);
-      tmem_ld_wait();
-      reg_fence(r, 128);
-      int valid;
-      if (j < nA) {
-        valid = a.La - j * BN;
-      } else {
-        valid = (a.mode == 1 ? row_end : a.Lb) - (j - nA) * BN;
-      }
-      if (valid < BN) {
-#pragma unroll
-        for (int c = 0; c < BN; ++c)
-          if (c >= valid) r[c] = __float_as_uint(-INFINITY);
-      }
-      float mx[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(r[i]);
-#pragma unroll
-      for (int c = 8; c < BN; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(r[c]));
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      const float m_new = fmaxf(m, mt * sl2);
-      if (j == 0) {
-        m = m_new;
-      } else if (__any_sync(0xffffffffu, m_new > m + kRescaleLog2)) {
-        const float alpha = (m_new == -INFINITY) ? 1.f : ex2(m - m_new);
+      if (pc.partial) {
+        // unnormalised O with its reference max and sum, merged by combine_kernel
+        const size_t rows_all = (size_t)2 * p.grid * (NQ * BM);
+        const size_t sr = (size_t)pc.slot * (NQ * BM) + w * BM + row;
+        float* po = p.part + sr * D;
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t o[32];
           tmem_ld32(tO + 32 * cc, o);
           tmem_ld_wait();
           reg_fence(o, 32);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tO + 32 * cc, o);
-        }
-        l *= alpha;
-        m = m_new;
-      }
-      const float mo = (m == -INFINITY) ? 0.f : m;
-      float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int c = half * 64 + 2 * i;
-          const float p0 = ex2(fmaf(__uint_as_float(r[c]), sl2, -mo));
-          const float p1 = ex2(fmaf(__uint_as_float(r[c + 1]), sl2, -mo));
-          ls[i & 3] += p0 + p1;
-          pk[i] = pack_bf16(p0, p1);
-        }
-        tmem_st32(tS + 32 * half, pk);
-      }
-      l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
-      tmem_st_wait();
-      tc_fence_before();
-      if (!(a.stall_inject && j == 0 && w == 0)) mbar_arrive(bP);
-    }
-    if (ok) ok = __all_sync(0xffffffffu, wait(bO, 0, ctl));
-    if (ok) {
-      tc_fence_after();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      const int64_t ob = ((int64_t)qrow * a.heads + head) * D;
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + ob;
-      float* outf = static_cast<float*>(a.out) + ob;
-#pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t o[32];
-        tmem_ld32(tO + 32 * cc, o);
-        tmem_ld_wait();
-        reg_fence(o, 32);
-        if (qrow < a.Lq && a.out_f32) {
-          float4* dst = reinterpret_cast<float4*>(outf + 32 * cc);
+          float4* dst = reinterpret_cast<float4*>(po + 32 * cc);
 #pragma unroll
           for (int v = 0; v < 8; ++v)
-            dst[v] = make_float4(__uint_as_float(o[4 * v + 0]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                                 __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
-        } else if (qrow < a.Lq) {
-          uint4* dst = reinterpret_cast<uint4*>(out + 32 * cc);
+            dst[v] = make_float4(__uint_as_float(o[4 * v + 0]), __uint_as_float(o[4 * v + 1]),
+                                 __uint_as_float(o[4 * v + 2]), __uint_as_float(o[4 * v + 3]));
+        }
+        p.part[rows_all * D + sr] = m;
+        p.part[rows_all * D + rows_all + sr] = l;
+      } else {
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const int64_t ob = ((int64_t)qrow * a.heads + head) * D;
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + ob;
+        float* outf = static_cast<float*>(a.out) + ob;
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * cc, o);
+          tmem_ld_wait();
+          reg_fence(o, 32);
+          if (qrow < a.Lq && a.out_f32) {
+            float4* dst = reinterpret_cast<float4*>(outf + 32 * cc);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 x;
-            x.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
-            x.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
-            x.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
-            x.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
-            dst[v] = x;
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(o[4 * v + 0]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                   __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+          } else if (qrow < a.Lq) {
+            uint4* dst = reinterpret_cast<uint4*>(out + 32 * cc);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 x;
+              x.x = pack_bf16(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv);
+              x.y = pack_bf16(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv);
+              x.z = pack_bf16(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv);
+              x.w = pack_bf16(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv);
+              dst[v] = x;
+            }
           }
         }
       }
+      tc_fence_before();
+      mbar_arrive(bOempty);
+      jt += n;
+      ++qi;
     }
   }
 
@@ -498,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
   __syncthreads();
   if (warp == 0 && lane == 0) {
     // copies still in flight land before the shared memory is released
-    wait_drain(bQ, 0);
+    if (q_issued > 0) wait_drain(bQfull, (q_issued - 1) & 1);
     const int first = tiles_issued > NS ? tiles_issued - NS : 0;
     for (int u = first; u < tiles_issued; ++u) wait_drain(bKVfull0 + 8 * (u % NS), (u / NS) & 1);
   }
@@ -516,7 +696,50 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
 }
 
 // ----------------------------------------------------------------------------
-// Host side: tensor maps and launch
+// Merge of split items: out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p
+// ----------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineParams c) {
+  constexpr int E = D / 32;
+  const int k = blockIdx.x;
+  const int r = blockIdx.y * 8 + (threadIdx.x >> 5);  // row within the item's 256 query rows
+  const int lane = threadIdx.x & 31;
+  const int item = c.item[k];
+  const int head = item / c.nqb;
+  const int qrow = (item - head * c.nqb) * NQ * BM + r;
+  if (qrow >= c.Lq) return;
+  const size_t rows_all = (size_t)2 * c.grid * (NQ * BM);
+  const float* pm = c.part + rows_all * D;
+  const float* pl = pm + rows_all;
+  float M = -INFINITY;
+  for (int i = c.first[k]; i < c.first[k + 1]; ++i) M = fmaxf(M, pm[(size_t)c.slot[i] * (NQ * BM) + r]);
+  float acc[E], L = 0.f;
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  for (int i = c.first[k]; i < c.first[k + 1]; ++i) {
+    const size_t sr = (size_t)c.slot[i] * (NQ * BM) + r;
+    const float mi = pm[sr];
+    const float wgt = (mi == -INFINITY) ? 0.f : exp2f(mi - M);
+    L += wgt * pl[sr];
+    const float* o = c.part + sr * D + lane * E;
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = fmaf(wgt, o[e], acc[e]);
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  const int64_t ob = ((int64_t)qrow * c.heads + head) * D + lane * E;
+  if (c.out_f32) {
+    float* out = static_cast<float*>(c.out) + ob;
+#pragma unroll
+    for (int e = 0; e < E; ++e) out[e] = acc[e] * inv;
+  } else {
+    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(c.out) + ob;
+#pragma unroll
+    for (int e = 0; e < E; ++e) out[e] = __float2bfloat16_rn(acc[e] * inv);
+  }
+}
+
+// ----------------------------------------------------------------------------
+// Host side: tensor maps, schedule and launch
 // ----------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -549,6 +772,50 @@ bool encode_tokens(CUtensorMap* m, const void* base, int L, int H, int D) {
   return encode3d(m, base, (uint64_t)D, (uint64_t)H, (uint64_t)L, (uint64_t)D * 2, (uint64_t)H * D * 2, 64, 1, 128);
 }
 
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  return n;
+}
+
+constexpr int kMinTailTiles = 16;  // shortest run of key tiles a tail CTA takes
+
+// Schedule of an attend launch (see "Work schedule"); fills p and the split list.
+void plan_attend(TcParams& p, CombineParams& cp, int max_ctas) {
+  const AttendArgs& a = p.a;
+  const int items = p.nqb * a.heads;
+  p.nkv = (a.La + BN - 1) / BN + (a.Lb + BN - 1) / BN;
+  int g = max_ctas < kMaxSplit ? max_ctas : kMaxSplit;
+  if (g > items) g = items;
+  if (g < 1) g = 1;
+  p.grid = g;
+  p.rounds = items / g;
+  const int rem = items - p.rounds * g;
+  p.tail_iters = (long long)rem * p.nkv;
+  long long tc = p.tail_iters / kMinTailTiles;
+  if (tc > g) tc = g;
+  if (tc < 1) tc = 1;
+  p.tail_ctas = rem > 0 ? (int)tc : 0;
+  cp.nsplit = 0;
+  int np = 0;
+  auto bnd = [&](long long cta) { return (p.tail_iters * cta) / p.tail_ctas; };
+  int c = 0;
+  for (int ti = 0; ti < rem; ++ti) {
+    const long long lo = (long long)ti * p.nkv, hi = lo + p.nkv;
+    while (c + 1 < p.tail_ctas && bnd(c + 1) <= lo) ++c;
+    int chi = c;
+    while (chi + 1 < p.tail_ctas && bnd(chi + 1) < hi) ++chi;
+    if (chi == c) continue;
+    const int k = cp.nsplit++;
+    cp.item[k] = p.rounds * p.grid + ti;
+    cp.first[k] = np;
+    cp.slot[np++] = 2 * c + (bnd(c) == lo ? 0 : 1);
+    for (int cc = c + 1; cc <= chi; ++cc) cp.slot[np++] = 2 * cc;
+  }
+  cp.first[cp.nsplit] = np;
+}
+
 template <int D>
 cudaError_t launch_tc(const AttendArgs& a, cudaStream_t stream) {
   TcParams p;
@@ -563,20 +830,98 @@ cudaError_t launch_tc(const AttendArgs& a, cudaStream_t stream) {
                 (uint64_t)a.cache_head_elems * 2, 64, 128, 1))
     return cudaErrorInvalidValue;
   p.nqb = (a.Lq + NQ * BM - 1) / (NQ * BM);
-  static bool attr_set = false;
-  if (!attr_set) {
+  CombineParams cp;
+  cp.nsplit = 0;
+  if (a.mode == 1) {
+    p.grid = p.nqb * a.heads;
+  } else {
+    // without scratch for two partial results per CTA, no item is split
+    int ctas = sm_count();
+    if (2 * ctas > a.scratch_slots) ctas = a.scratch_slots / 2;
+    plan_attend(p, cp, ctas < 1 ? 1 : ctas);
+    if (cp.nsplit > 0 && !a.scratch) return cudaErrorInvalidValue;
+    p.part = a.scratch;
+  }
+  static int attr_done[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
     cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          Cfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    if (dev >= 0 && dev < 64) attr_done[dev] = 1;
   }
-  const unsigned grid = (unsigned)(p.nqb * a.heads);
-  attend_tc_kernel<D><<<grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(p);
+  attend_tc_kernel<D><<<(unsigned)p.grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(p);
+  count_launch();
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || cp.nsplit == 0) return e;
+  cp.out = a.out;
+  cp.part = p.part;
+  cp.grid = p.grid;
+  cp.nqb = p.nqb;
+  cp.Lq = a.Lq;
+  cp.heads = a.heads;
+  cp.out_f32 = a.out_f32;
+  combine_kernel<D><<<dim3((unsigned)cp.nsplit, (NQ * BM) / 8), 256, 0, stream>>>(cp);
   count_launch();
   return cudaGetLastError();
 }
 
 }  // namespace
+
+size_t attend_scratch_bytes(int head_dim, int slots) {
+  return (size_t)slots * (NQ * BM) * (head_dim + 2) * sizeof(float);
+}
+
+int attend_scratch_slots_wanted() {
+  int n = sm_count();
+  if (n > kMaxSplit) n = kMaxSplit;
+  return 2 * n;
+}
+
+int attend_schedule_dump(int Lq, int La, int Lb, int heads, int max_ctas, int* grid, int* out, int cap,
+                         int* splits, int split_cap, int* split_ints) {
+  TcParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.a.Lq = Lq;
+  p.a.La = La;
+  p.a.Lb = Lb;
+  p.a.heads = heads;
+  p.nqb = (Lq + NQ * BM - 1) / (NQ * BM);
+  CombineParams cp;
+  plan_attend(p, cp, max_ctas);
+  *grid = p.grid;
+  int n = 0;
+  for (int c = 0; c < p.grid; ++c) {
+    Walker wk;
+    walker_init(wk, p, c);
+    Piece pc;
+    while (walker_next(wk, p, pc, c)) {
+      if (n + 6 <= cap) {
+        out[n + 0] = c;
+        out[n + 1] = pc.item;
+        out[n + 2] = pc.j0;
+        out[n + 3] = pc.j1;
+        out[n + 4] = pc.partial;
+        out[n + 5] = pc.slot;
+      }
+      n += 6;
+    }
+  }
+  // split list: item, number of parts, then the parts' slots
+  int m = 0;
+  for (int k = 0; k < cp.nsplit; ++k) {
+    const int cnt = cp.first[k + 1] - cp.first[k];
+    if (m + 2 + cnt <= split_cap) {
+      splits[m] = cp.item[k];
+      splits[m + 1] = cnt;
+      for (int i = 0; i < cnt; ++i) splits[m + 2 + i] = cp.slot[cp.first[k] + i];
+    }
+    m += 2 + cnt;
+  }
+  *split_ints = m;
+  return n / 6;
+}
 
 cudaError_t launch_attend_bf16_tc(const AttendArgs& a, cudaStream_t stream) {
   return a.head_dim == 64 ? launch_tc<64>(a, stream) : launch_tc<128>(a, stream);

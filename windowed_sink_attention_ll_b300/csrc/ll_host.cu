@@ -39,6 +39,8 @@ struct ll_cache {
   std::vector<int64_t> fos;             // frame_of_slot, L x (S+W)
   unsigned* err_host = nullptr;         // mapped host word written by kernels
   unsigned* err_dev = nullptr;
+  float* scratch = nullptr;             // partial results of split attention work items
+  int scratch_slots = 0;
   int stall_inject = 0;
   int stall_timeout_us = 0;
   int use_simt = 0;
@@ -96,6 +98,8 @@ ll::AttendArgs base_args(ll_cache* c, int layer) {
   a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)c->D));
   a.err = c->err_dev;
   a.out_f32 = (c->dtype == LL_FP32 || c->out_f32) ? 1 : 0;
+  a.scratch = c->scratch;
+  a.scratch_slots = c->scratch_slots;
   a.stall_inject = c->stall_inject;
   a.timeout_ns = c->stall_inject ? (long long)c->stall_timeout_us * 1000LL : kDefaultTimeoutNs;
   c->stall_inject = 0;  // one launch only
@@ -262,12 +266,26 @@ ll_status ll_cache_create(ll_cache** out, int layers, int heads, int head_dim, i
       return LL_ERR_CUDA;
     }
   }
+  if (dtype == LL_BF16) {
+    // the tensor-core kernel splits left-over work items across SMs and merges
+    // their partial results: two slots per SM
+    c->scratch_slots = ll::attend_scratch_slots_wanted();
+    if (cudaMalloc(reinterpret_cast<void**>(&c->scratch), ll::attend_scratch_bytes(head_dim, c->scratch_slots)) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(c->k);
+      cudaFree(c->v);
+      delete c;
+      return LL_ERR_OOM;
+    }
+  }
   if (cudaHostAlloc(reinterpret_cast<void**>(&c->err_host), 256, cudaHostAllocMapped) != cudaSuccess ||
       cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->err_dev), c->err_host, 0) != cudaSuccess) {
     cudaGetLastError();
     if (c->err_host) cudaFreeHost(c->err_host);
     cudaFree(c->k);
     cudaFree(c->v);
+    cudaFree(c->scratch);
     delete c;
     return LL_ERR_CUDA;
   }
@@ -287,6 +305,7 @@ void ll_cache_destroy(ll_cache* c) {
   for (auto e : c->event_pool) cudaEventDestroy(e);
   cudaFree(c->k);
   cudaFree(c->v);
+  cudaFree(c->scratch);
   cudaFreeHost(c->err_host);
   delete c;
 }
@@ -469,6 +488,12 @@ ll_status ll_profile_read(ll_cache* c, int kind, int64_t* launches, double* tota
   if (launches) *launches = n;
   if (total_ms) *total_ms = ms;
   return LL_OK;
+}
+
+int ll_debug_attend_schedule(int Lq, int La, int Lb, int heads, int max_ctas, int* grid, int* pieces, int cap,
+                             int* splits, int split_cap, int* split_ints) {
+  if (Lq < 1 || La < 0 || Lb < 1 || heads < 1 || max_ctas < 1 || !grid || !split_ints) return -1;
+  return ll::attend_schedule_dump(Lq, La, Lb, heads, max_ctas, grid, pieces, cap, splits, split_cap, split_ints);
 }
 
 ll_status ll_debug_use_simt(ll_cache* c, int enable) {
