@@ -213,6 +213,61 @@ LL_API ll_status ll_debug_use_simt(ll_cache* cache, int enable);
 LL_API int ll_debug_attend_schedule(int Lq, int La, int Lb, int heads, int max_ctas, int* grid, int* pieces,
                                     int cap, int* splits, int split_cap, int* split_ints);
 
+/*
+ * ll_attend_chunk_noalloc -- the attention of ll_attend_chunk (no commit) for
+ * callers that may not allocate device memory.  The paper has no counterpart:
+ * this entry point exists for deployment.
+ *
+ * Who cannot allocate: a host program whose memory manager owns the GPU's
+ * whole budget (e.g. a serving runtime that reserves nearly all of HBM in its
+ * own pool and hands out slices: a cudaMalloc behind its back fails or breaks
+ * its accounting), a plugin interface that hands a library a stream and
+ * buffers and forbids it to allocate, and real-time loops whose per-frame
+ * deadline cannot absorb cudaMalloc / cudaFree, which may block the host and
+ * synchronise the device.  ll_cache_create allocates, so these callers keep
+ * the cache in memory they own and place frames with ll_frame_slot /
+ * ll_resident_frames.  This call allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ *
+ * Per head h: out_h = softmax(q_h K_h^T / sqrt(d)) V_h over the keys
+ * [cached rows || the chunk's own rows], bf16 in and out, fp32 softmax.
+ *   q, k, v, out: [chunk_tokens][heads][head_dim] bf16 device buffers (16-byte
+ *                 aligned; out may not alias q, k or v).
+ *   k_cached, v_cached: the resident rows, head-major: head h's cached_tokens
+ *                 rows of head_dim elements start at element
+ *                 h * cached_head_stride (16-byte aligned, stride a multiple
+ *                 of 8).  The cache layout of ll_cache_read qualifies, with
+ *                 the resident frames in slots [0, R) and
+ *                 cached_tokens = R * T.  Ignored when cached_tokens = 0.
+ *   err_word: optional device-visible 4-byte word; a device wait that runs
+ *             out (2 s) writes 1 into it and out is then undefined.  The
+ *             caller zeroes it and reads it after the stream completes.
+ *             NULL: such an event is not reported.
+ *   stream: CUDA stream (cudaStream_t) of the work.
+ * The scratch for the split work items' partial results is a file-scope
+ * device array of LL_NOALLOC_SCRATCH_BYTES (37.6 MiB), which every GPU that
+ * loads the library holds until the process exits: two partial results of 256
+ * query rows per CTA for up to LL_NOALLOC_PARTIAL_SLOTS / 2 = 148 CTAs at
+ * head_dim 128 (one per SM of a B300; 291 CTAs at head_dim 64).  A request that
+ * would need more (a GPU with more SMs and more work items than that) returns
+ * LL_ERR_UNSUPPORTED before anything is enqueued; so do head_dim not in
+ * {64, 128} and cached_tokens + chunk_tokens > 2^30.  Bad pointers, strides or
+ * sizes return LL_ERR_INVALID_ARG.
+ * The first call on a device, with that device current, looks up the array's
+ * device address (cudaGetSymbolAddress); make it before any stream capture.
+ * Every call on a device shares the array, and it keeps the previous call's
+ * contents: nothing in it needs to start at zero, since each call writes
+ * every partial result it later reads.  Calls whose work may overlap on the
+ * GPU (unordered streams, other host threads) race on the array and give
+ * wrong results: order them, e.g. on one stream.
+ */
+#define LL_NOALLOC_PARTIAL_SLOTS 296
+#define LL_NOALLOC_SCRATCH_BYTES (256 + (size_t)LL_NOALLOC_PARTIAL_SLOTS * 256 * 130 * 4)
+LL_API ll_status ll_attend_chunk_noalloc(const void* q, const void* k_cached, const void* v_cached,
+                                         int cached_tokens, int64_t cached_head_stride, const void* k,
+                                         const void* v, int chunk_tokens, void* out, int heads, int head_dim,
+                                         unsigned* err_word, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

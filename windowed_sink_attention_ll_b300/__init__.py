@@ -36,7 +36,7 @@ EXPORTS = ("ll_status_str", "ll_cache_create", "ll_cache_destroy", "ll_attend_ch
            "ll_recache_attend", "ll_reset", "ll_cache_state", "ll_cache_read", "ll_sync",
            "ll_cache_info", "ll_frame_slot", "ll_resident_frames", "ll_launch_count",
            "ll_debug_inject_stall", "ll_debug_use_simt", "ll_profile_enable", "ll_profile_read",
-           "ll_set_output_dtype", "ll_debug_attend_schedule")
+           "ll_set_output_dtype", "ll_debug_attend_schedule", "ll_attend_chunk_noalloc")
 LL_KERNEL_ATTEND, LL_KERNEL_PREFILL, LL_KERNEL_COPY = 0, 1, 2
 
 
@@ -82,6 +82,7 @@ def _lib() -> ctypes.CDLL:
                                                ctypes.POINTER(i32), i32, ctypes.POINTER(i32), i32,
                                                ctypes.POINTER(i32)]),
             "ll_profile_read": (i32, [vp, i32, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]),
+            "ll_attend_chunk_noalloc": (i32, [vp, vp, vp, i32, i64, vp, vp, i32, vp, i32, i32, vp, vp]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -308,3 +309,39 @@ def ll_debug_attend_schedule(Lq: int, La: int, Lb: int, heads: int, max_ctas: in
         sp.append((splits[i], list(splits[i + 2:i + 2 + cnt])))
         i += 2 + cnt
     return grid.value, out, sp
+
+
+def ll_attend_chunk_noalloc(q, k_cached, v_cached, cached_tokens: int, k, v, out, err_word=None,
+                            stream=None) -> None:
+    """Chunk attention without any device allocation (see include/ll.h).
+
+    q, k, v, out: contiguous bf16 CUDA tensors [chunk_tokens, H, d].
+    k_cached, v_cached: bf16 CUDA tensors [H, rows, d] with contiguous rows per
+    head (rows >= cached_tokens), e.g. a layer of ll_cache_read reshaped to
+    [H, (S+W)*T, d]; None when cached_tokens is 0.  err_word: optional int32
+    CUDA tensor of one element that a timed-out device wait sets to 1.
+    """
+    L, H, d = (tuple(q.shape) + (0, 0, 0))[:3]
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()
+                and tuple(t.shape) == (L, H, d)):
+            raise ValueError("%s must be a contiguous bf16 CUDA tensor of shape %s" % (n, (L, H, d)))
+    kc = vc = None
+    stride = 0
+    if cached_tokens > 0:
+        for t, n in ((k_cached, "k_cached"), (v_cached, "v_cached")):
+            if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16 and t.dim() == 3
+                    and t.shape[0] == H and t.shape[1] >= cached_tokens and t.shape[2] == d
+                    and t.stride(2) == 1 and t.stride(1) == d):
+                raise ValueError("%s must be a bf16 CUDA tensor [H, >= cached_tokens, d] with contiguous rows" % n)
+        if k_cached.stride(0) != v_cached.stride(0):
+            raise ValueError("k_cached and v_cached must have the same head stride")
+        kc, vc, stride = k_cached.data_ptr(), v_cached.data_ptr(), k_cached.stride(0)
+    ew = None
+    if err_word is not None:
+        if not (isinstance(err_word, torch.Tensor) and err_word.is_cuda and err_word.dtype == torch.int32):
+            raise ValueError("err_word must be an int32 CUDA tensor")
+        ew = err_word.data_ptr()
+    _check(_lib().ll_attend_chunk_noalloc(q.data_ptr(), kc, vc, cached_tokens, stride, k.data_ptr(), v.data_ptr(),
+                                          L, out.data_ptr(), H, d, ew, _stream(stream)),
+           "ll_attend_chunk_noalloc")
