@@ -254,6 +254,83 @@ def oracle_rate(shape: llsynth.Shape, budget_s: float = 12.0):
 # our arm
 # ----------------------------------------------------------------------------
 
+def timed_region(args, world, local, caches, step):
+    """W warm-up steps, then exactly K timed steps between barriers and synchronisations.
+
+    Returns (ms, clocks, launches, per-kind (launches, ms) summed over ``caches``)."""
+    import windowed_sink_attention_ll_b300 as ll
+
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    kinds = (ll.LL_KERNEL_ATTEND, ll.LL_KERNEL_PREFILL, ll.LL_KERNEL_COPY)
+    for cache in caches:
+        for kind in kinds:
+            ll.ll_profile_read(cache, kind)
+        ll.ll_profile_enable(cache, True)
+    launches0 = ll.ll_launch_count()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    launches = ll.ll_launch_count() - launches0
+    prof = {}
+    for cache in caches:
+        ll.ll_profile_enable(cache, False)
+        for kind in kinds:
+            n, ms_k = ll.ll_profile_read(cache, kind)
+            a, b = prof.get(kind, (0, 0.0))
+            prof[kind] = (a + n, b + ms_k)
+    return ev0.elapsed_time(ev1), clk.summary(), launches, prof
+
+
+def tensor_roofline(kernel, flops, n, ms, pk, pk_src, sustained=True):
+    """Tensor-bound roofline object of one kernel: flops over its summed CUDA-event time."""
+    achieved = flops / (ms / 1e3) / 1e12 if ms > 0 else 0.0
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    peak = pk.get(key, FALLBACK[key])
+    return {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak,
+            "peak_source": "%s %s (%s)" % (pk_src, key, "kernel timed inside a long step" if sustained
+                                           else "kernel timed in isolation"),
+            "frac_of_burst_peak": achieved / pk.get("bf16_tflops", FALLBACK["bf16_tflops"]),
+            "frac_of_nominal_2250": achieved / 2250.0,
+            "launches": n, "ms_per_launch": ms / max(n, 1), "flops_per_launch": flops / max(n, 1)}
+
+
+def hbm_roofline(kernel, nbytes, n, ms, pk):
+    achieved = nbytes / (ms / 1e3) / 1e9 if ms > 0 else 0.0
+    peak = pk.get("hbm_gbs", FALLBACK["hbm_gbs"])
+    return {"kernel": kernel, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+            "frac": achieved / peak, "frac_of_nominal_8000": achieved / 8000.0, "launches": n,
+            "us_per_launch": 1e3 * ms / max(n, 1), "bytes_per_launch": nbytes / max(n, 1)}
+
+
+def base_result(args, world, value, ms_max, config):
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) q/k/v per layer and chunk, Wan2.1-1.3B shapes; no weights)",
+        "config": config,
+    }
+
+
+def shape_config(shape, extra):
+    cfg = {"layers": shape.layers, "heads": shape.heads, "head_dim": shape.head_dim,
+           "tokens_per_frame": shape.tokens_per_frame, "sink_frames": shape.sink_frames,
+           "window_frames": shape.window_frames, "chunk_frames": shape.chunk_frames}
+    cfg.update(extra)
+    return cfg
+
+
 def run_ours(args, world, rank, local):
     import windowed_sink_attention_ll_b300 as ll
 
@@ -281,72 +358,28 @@ def run_ours(args, world, rank, local):
                 q, k, v = inputs[l][c]
                 ll.ll_attend_chunk(cache, l, q, k, v, outs[l], True, stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    for kind in (ll.LL_KERNEL_ATTEND, ll.LL_KERNEL_COPY, ll.LL_KERNEL_PREFILL):
-        ll.ll_profile_read(cache, kind)
-    ll.ll_profile_enable(cache, True)
-    launches0 = ll.ll_launch_count()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
-        barrier(world)
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        for _ in range(args.steps):
-            step()
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-    ll.ll_profile_enable(cache, False)
-    launches = ll.ll_launch_count() - launches0
-    ms = ev0.elapsed_time(ev1)
+    ms, clocks, launches, prof = timed_region(args, world, local, [cache], step)
     ms_max = max_over_ranks(ms, world)
-    n_att, ms_att = ll.ll_profile_read(cache, ll.LL_KERNEL_ATTEND)
-    n_cp, ms_cp = ll.ll_profile_read(cache, ll.LL_KERNEL_COPY)
-
+    n_att, ms_att = prof[ll.LL_KERNEL_ATTEND]
+    n_cp, ms_cp = prof[ll.LL_KERNEL_COPY]
     pk, pk_src = peaks()
-    tflops_att = step_flops * args.steps / (ms_att / 1e3) / 1e12
-    peak_t = pk.get("bf16_tflops_sustained", FALLBACK["bf16_tflops_sustained"])
-    gbs_cp = step_append * args.steps / (ms_cp / 1e3) / 1e9
-    traffic = traffic_per_launch()
-    result = {
-        "metric": METRIC,
-        "value": step_frames * args.steps * world / (ms_max / 1e3),
-        "unit": UNIT,
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": ms_max / args.steps,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) q/k/v per layer and chunk, Wan2.1-1.3B shapes; no weights)",
-        "config": {"workload": "stream30: 30 layers x 20 chunks (60 latent frames), H=12, d=128, "
-                               "T=1560, C=3, S=3, W=9, 1 committed pass per chunk",
-                   "layers": shape.layers, "chunks": chunks, "heads": H, "head_dim": d,
-                   "tokens_per_frame": T, "sink_frames": S, "window_frames": W, "chunk_frames": C,
-                   "l2": "inputs larger than L2 (%.1f GB q/k/v + %.2f GB cache per rank)" % (
-                       3 * L * H * d * 2 * chunks * shape.layers / 1e9, 2 * shape.layers * (S + W) * T * H * d * 2 / 1e9),
-                   "parallelism": "replicas x%d (independent streams, no collective)" % world},
+    config = {"workload": "stream30: 30 layers x 20 chunks (60 latent frames), H=12, d=128, "
+                          "T=1560, C=3, S=3, W=9, 1 committed pass per chunk"}
+    config.update(shape_config(shape, {
+        "chunks": chunks,
+        "l2": "inputs larger than L2 (%.1f GB q/k/v + %.2f GB cache per rank)" % (
+            3 * L * H * d * 2 * chunks * shape.layers / 1e9, 2 * shape.layers * (S + W) * T * H * d * 2 / 1e9),
+        "parallelism": "replicas x%d (independent streams, no collective)" % world}))
+    result = base_result(args, world, step_frames * args.steps * world / (ms_max / 1e3), ms_max, config)
+    roof = tensor_roofline("attend_tc_kernel<128>", step_flops * args.steps, n_att, ms_att, pk, pk_src)
+    roof["traffic"] = traffic_per_launch()
+    result.update({
         "tflops": step_flops * args.steps * world / (ms_max / 1e3) / 1e12,
-        "roofline": {"kernel": "attend_tc_kernel<128>", "bound": "tensor", "achieved": tflops_att,
-                     "peak": peak_t, "unit": "TFLOP/s", "frac": tflops_att / peak_t,
-                     "peak_source": "%s bf16_tflops_sustained (kernel timed inside a long step)" % pk_src,
-                     "frac_of_burst_peak": tflops_att / pk.get("bf16_tflops", FALLBACK["bf16_tflops"]),
-                     "frac_of_nominal_2250": tflops_att / 2250.0,
-                     "launches": n_att, "ms_per_launch": ms_att / max(n_att, 1),
-                     "flops_per_launch": step_flops * args.steps / max(n_att, 1),
-                     "traffic": traffic},
-        "append": {"kernel": "copy_frames_kernel", "bound": "hbm", "achieved": gbs_cp,
-                   "peak": pk.get("hbm_gbs", FALLBACK["hbm_gbs"]), "unit": "GB/s",
-                   "frac": gbs_cp / pk.get("hbm_gbs", FALLBACK["hbm_gbs"]), "frac_of_nominal_8000": gbs_cp / 8000.0,
-                   "launches": n_cp, "us_per_launch": 1e3 * ms_cp / max(n_cp, 1),
-                   "bytes_per_launch": step_append * args.steps / max(n_cp, 1)},
+        "roofline": roof,
+        "append": hbm_roofline("copy_frames_kernel", step_append * args.steps, n_cp, ms_cp, pk),
         "gpu_launches": launches,
-        "clocks": clk.summary(),
-    }
+        "clocks": clocks,
+    })
     if not args.no_e2e:
         result["e2e"] = run_e2e(ll, cache, shape, chunks, step_frames, world, rank, args)
     cache.close()
@@ -355,6 +388,162 @@ def run_ours(args, world, rank, local):
         rate, threads, sample = oracle_rate(shape)
         result["cpu_baseline"] = {"value": step_frames / (step_flops / rate), "unit": UNIT, "cores": threads,
                                   "kind": "oracle", "sample": sample}
+    return result
+
+
+def run_single(args, world, rank, local):
+    """Single Wan-shaped layer at steady state (23400 keys): one step = 4 query passes of a
+    chunk, the last one committing (per-head input scales 0.5-2.0)."""
+    import windowed_sink_attention_ll_b300 as ll
+
+    shape = llsynth.SINGLE_LAYER
+    H, d, T, S, W, C = (shape.heads, shape.head_dim, shape.tokens_per_frame, shape.sink_frames,
+                        shape.window_frames, shape.chunk_frames)
+    L = C * T
+    passes = llsynth.SINGLE_LAYER_PASSES
+    cache = ll.ll_cache_create(1, H, d, T, S, W, C, ll.LL_BF16)
+    for c in range((S + W) // C):
+        q, k, v = (llsynth.seeded_normal(("bench-single-fill", rank, c, t), (L, H, d), device="cuda",
+                                         per_head_scale=True) for t in "qkv")
+        ll.ll_attend_chunk(cache, 0, q, k, v, torch.empty_like(q), True)
+    pool = 8  # distinct chunks cycled (8 x 4 passes x 43 MB of q/k/v: far beyond L2)
+    inputs = [[tuple(llsynth.seeded_normal(("bench-single", rank, i, p, t), (L, H, d), device="cuda",
+                                           per_head_scale=True) for t in "qkv") for p in range(passes)]
+              for i in range(pool)]
+    out = torch.empty((L, H, d), dtype=torch.bfloat16, device="cuda")
+    lkv = (S + W + C) * T
+    pass_flops = attend_flops(L, lkv, H, d)
+    it = [0]
+
+    def step():
+        chunk = inputs[it[0] % pool]
+        it[0] += 1
+        for p in range(passes):
+            ll.ll_attend_chunk(cache, 0, *chunk[p], out, p == passes - 1)
+
+    ms, clocks, launches, prof = timed_region(args, world, local, [cache], step)
+    ms_max = max_over_ranks(ms, world)
+    n_att, ms_att = prof[ll.LL_KERNEL_ATTEND]
+    n_cp, ms_cp = prof[ll.LL_KERNEL_COPY]
+    pk, pk_src = peaks()
+    config = {"workload": "single: 1 Wan-shaped layer at steady state, H=12, d=128, T=1560, C=3, S=3, W=9, "
+                          "Lkv=23400, 4 passes per chunk (commit on the last), per-head scales 0.5-2.0"}
+    config.update(shape_config(shape, {"passes": passes, "l2": "8 distinct chunks cycled (1.4 GB of q/k/v)"}))
+    result = base_result(args, world, C * args.steps * world / (ms_max / 1e3), ms_max, config)
+    roof = tensor_roofline("attend_tc_kernel<128>", pass_flops * passes * args.steps, n_att, ms_att, pk, pk_src,
+                           sustained=False)
+    roof["traffic"] = traffic_per_launch()
+    result.update({
+        "tflops": pass_flops * passes * args.steps * world / (ms_max / 1e3) / 1e12,
+        "roofline": roof,
+        "append": hbm_roofline("copy_frames_kernel", append_bytes(shape, C) * args.steps, n_cp, ms_cp, pk),
+        "gpu_launches": launches, "clocks": clocks,
+    })
+    cache.close()
+    return result
+
+
+def run_recache30(args, world, rank, local):
+    """30 layers x 40 chunks with a recache prefill of the 12 resident frames in every layer
+    before chunks 10, 20 and 30 (prompt switches)."""
+    import windowed_sink_attention_ll_b300 as ll
+
+    shape = llsynth.RECACHE30
+    chunks = llsynth.RECACHE30_CHUNKS
+    H, d, T, S, W, C = (shape.heads, shape.head_dim, shape.tokens_per_frame, shape.sink_frames,
+                        shape.window_frames, shape.chunk_frames)
+    L = C * T
+    R = S + W
+    pool = 20  # chunk inputs cycled per layer (26 GB in total: far beyond L2)
+    inputs = [[tuple(llsynth.seeded_normal(("bench-rc", rank, l, c, t), (L, H, d), device="cuda") for t in "qkv")
+               for c in range(pool)] for l in range(shape.layers)]
+    rc_inputs = [[tuple(llsynth.seeded_normal(("bench-rc-win", rank, l, sw, t), (R * T, H, d), device="cuda")
+                        for t in "qkv") for sw in range(len(llsynth.RECACHE30_SWITCHES))]
+                 for l in range(shape.layers)]
+    outs = [torch.empty((L, H, d), dtype=torch.bfloat16, device="cuda") for _ in range(shape.layers)]
+    out_rc = torch.empty((R * T, H, d), dtype=torch.bfloat16, device="cuda")
+    cache = ll.ll_cache_create(shape.layers, H, d, T, S, W, C, ll.LL_BF16)
+    stream = torch.cuda.current_stream()
+    plan = stream_plan(shape, chunks)
+    att_flops = sum(attend_flops(L, lkv, H, d) for _, lkv in plan) * shape.layers
+    # block-causal prefill over R frames in blocks of C frames: block g sees blocks 0..g
+    nb = R // C
+    pre_flops = 4.0 * (C * T) ** 2 * (nb * (nb + 1) // 2) * H * d
+    switches = len(llsynth.RECACHE30_SWITCHES)
+    step_pre_flops = pre_flops * shape.layers * switches
+
+    def step():
+        ll.ll_reset(cache)
+        for c in range(chunks):
+            if c in llsynth.RECACHE30_SWITCHES:
+                sw = llsynth.RECACHE30_SWITCHES.index(c)
+                for l in range(shape.layers):
+                    ll.ll_recache_attend(cache, l, *rc_inputs[l][sw], out_rc, stream)
+            for l in range(shape.layers):
+                ll.ll_attend_chunk(cache, l, *inputs[l][c % pool], outs[l], True, stream)
+
+    ms, clocks, launches, prof = timed_region(args, world, local, [cache], step)
+    ms_max = max_over_ranks(ms, world)
+    pk, pk_src = peaks()
+    n_att, ms_att = prof[ll.LL_KERNEL_ATTEND]
+    n_pre, ms_pre = prof[ll.LL_KERNEL_PREFILL]
+    config = {"workload": "recache30: 30 layers x 40 chunks (120 latent frames), recache prefill of 12 frames "
+                          "(18720 tokens, block-causal in 3-frame blocks) in every layer before chunks 10, 20, 30"}
+    config.update(shape_config(shape, {"chunks": chunks, "switches": list(llsynth.RECACHE30_SWITCHES),
+                                       "l2": "inputs larger than L2 (41 GB per rank)"}))
+    result = base_result(args, world, chunks * C * args.steps * world / (ms_max / 1e3), ms_max, config)
+    result.update({
+        "tflops": (att_flops + step_pre_flops) * args.steps * world / (ms_max / 1e3) / 1e12,
+        "roofline": tensor_roofline("attend_tc_kernel<128>", att_flops * args.steps, n_att, ms_att, pk, pk_src),
+        "prefill": dict(tensor_roofline("attend_tc_kernel<128> (prefill mode)", step_pre_flops * args.steps, n_pre,
+                                        ms_pre, pk, pk_src),
+                        ms_per_switch_30_layers=ms_pre / max(1, args.steps * switches)),
+        "gpu_launches": launches, "clocks": clocks,
+    })
+    cache.close()
+    return result
+
+
+def run_sweep(args, world, rank, local):
+    """Window/sink sweep: steady-state chunk attend TFLOPS for W in {3,6,9,12,18} x S in {0,3}."""
+    import windowed_sink_attention_ll_b300 as ll
+
+    base = llsynth.WAN
+    H, d, T, C = base["heads"], base["head_dim"], base["tokens_per_frame"], base["chunk_frames"]
+    L = C * T
+    pool = 8
+    inputs = [tuple(llsynth.seeded_normal(("bench-sweep", rank, i, t), (L, H, d), device="cuda") for t in "qkv")
+              for i in range(pool)]
+    out = torch.empty((L, H, d), dtype=torch.bfloat16, device="cuda")
+    pk, pk_src = peaks()
+    rows, total_ms, total_frames = [], 0.0, 0
+    for W in llsynth.SWEEP_W:
+        for S in llsynth.SWEEP_S:
+            cache = ll.ll_cache_create(1, H, d, T, S, W, C, ll.LL_BF16)
+            while ll.ll_cache_state(cache, 0)[0] < S + W + C:  # steady state: sink and window full
+                ll.ll_attend_chunk(cache, 0, *inputs[0], out, True)
+            lkv = (S + W + C) * T
+            it = [0]
+
+            def step():
+                for _ in range(10):
+                    ll.ll_attend_chunk(cache, 0, *inputs[it[0] % pool], out, True)
+                    it[0] += 1
+
+            ms, clocks, launches, prof = timed_region(args, world, local, [cache], step)
+            n_att, ms_att = prof[ll.LL_KERNEL_ATTEND]
+            flops = attend_flops(L, lkv, H, d) * 10 * args.steps
+            rows.append({"W": W, "S": S, "Lkv": lkv, "ms_per_chunk": ms / (10 * args.steps),
+                         "attend_tflops": flops / (ms_att / 1e3) / 1e12,
+                         "attend_frac_of_burst": flops / (ms_att / 1e3) / 1e12 / pk.get("bf16_tflops", 1800.0)})
+            total_ms += ms
+            total_frames += 10 * C * args.steps
+            cache.close()
+    ms_max = max_over_ranks(total_ms, world)
+    config = {"workload": "sweep: 1 Wan-shaped layer, W in {3,6,9,12,18} x S in {0,3}, steady state, "
+                          "10 committed chunks per step and setting"}
+    result = base_result(args, world, total_frames * world / (ms_max / 1e3), ms_max, config)
+    result.update({"sweep": rows, "clocks": clocks})
     return result
 
 
@@ -460,6 +649,9 @@ def main():
     ap.add_argument("--steps", type=int, default=5)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["stream30", "single", "recache30", "sweep"], default="stream30",
+                    help="stream30 (default: the 30-layer stack the metric names); the others time the "
+                         "single-layer, prompt-switch recache and window/sink sweep workloads")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -473,7 +665,8 @@ def main():
             print(json.dumps(run_reference(args, world, rank)), flush=True)
         return
     world, rank, local = dist_setup()
-    res = run_ours(args, world, rank, local)
+    run = {"stream30": run_ours, "single": run_single, "recache30": run_recache30, "sweep": run_sweep}
+    res = run[args.workload](args, world, rank, local)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
