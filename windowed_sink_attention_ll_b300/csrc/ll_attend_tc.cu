@@ -228,6 +228,30 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// max of three floats in one instruction
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+// (d0, d1) = (a0, a1) * b + c, two lanes per instruction
+__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, uint64_t b, uint64_t c) {
+  asm("{\n\t.reg .b64 a, d;\n\tmov.b64 a, {%2, %3};\n\tfma.rn.f32x2 d, a, %4, %5;\n\tmov.b64 {%0, %1}, d;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "l"(b), "l"(c));
+}
+// s0 += low bf16 of pk, s1 += high bf16 of pk (widened exactly, fp32 adds)
+__device__ __forceinline__ void add_bf16x2(float& s0, float& s1, uint32_t pk) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tadd.rn.f32.bf16 %0, lo, %0;\n\t"
+      "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "r"(pk));
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
@@ -547,26 +571,37 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         ok = __all_sync(0xffffffffu, wait(bS, (jt + t) & 1, ctl));
         if (!ok) break;
         tc_fence_after();
+        // S in two halves: the max of the first 64 columns overlaps the load of the rest
         uint32_t r[BN];
         tmem_ld32(tS + 0, r + 0);
         tmem_ld32(tS + 32, r + 32);
+        tmem_ld_wait();
+        reg_fence(r, BN / 2);
         tmem_ld32(tS + 64, r + 64);
         tmem_ld32(tS + 96, r + 96);
-        tmem_ld_wait();
-        reg_fence(r, BN);
         const int valid = j < nA ? a.La - j * BN : (a.mode == 1 ? row_end : a.Lb) - (j - nA) * BN;
-        if (valid < BN) {
+        if (valid < BN / 2) {
 #pragma unroll
-          for (int c = 0; c < BN; ++c)
+          for (int c = 0; c < BN / 2; ++c)
             if (c >= valid) r[c] = __float_as_uint(-INFINITY);
         }
-        float mx[8];
+        float mx[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = __uint_as_float(r[i]);
+        for (int i = 0; i < 4; ++i) mx[i] = __uint_as_float(r[i]);
 #pragma unroll
-        for (int c = 8; c < BN; ++c) mx[c & 7] = fmaxf(mx[c & 7], __uint_as_float(r[c]));
-        const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                               fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+        for (int c = 4; c < BN / 2; c += 2)
+          mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+        tmem_ld_wait();
+        reg_fence(r + BN / 2, BN / 2);
+        if (valid < BN) {
+#pragma unroll
+          for (int c = BN / 2; c < BN; ++c)
+            if (c >= valid) r[c] = __float_as_uint(-INFINITY);
+        }
+#pragma unroll
+        for (int c = BN / 2; c < BN; c += 2)
+          mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
+        const float mt = max3f(max3f(mx[0], mx[1], mx[2]), mx[3], -INFINITY);
         const float m_new = fmaxf(m, mt * sl2);
         // the reference max moves (and O is rescaled, after P is written) only
         // when some row of the warp grew by more than 2^8
@@ -581,21 +616,24 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         // P = 2^(s*log2e/sqrt(d) - m), rounded to bf16 for the P V product.  The
         // row sum adds the same rounded values, so numerator and denominator
         // carry the same rounding and a dominant key keeps its exact weight.
-        float ls[4] = {0.f, 0.f, 0.f, 0.f};
+        // two columns per packed fma; the row sum adds the bf16 halves of each
+        // packed P word directly (exact widening, fp32 add)
+        const uint64_t sl2x2 = pack_f32x2(sl2, sl2), nmo2 = pack_f32x2(-mo, -mo);
+        float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int g = 0; g < BN / 32; ++g) {
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int c = g * 32 + 2 * i;
-            const float p0 = ex2(fmaf(__uint_as_float(r[c]), sl2, -mo));
-            const float p1 = ex2(fmaf(__uint_as_float(r[c + 1]), sl2, -mo));
-            pk[i] = pack_bf16(p0, p1);
-            ls[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xFFFF0000u);
+            float x0, x1;
+            fma_f32x2(x0, x1, __uint_as_float(r[c]), __uint_as_float(r[c + 1]), sl2x2, nmo2);
+            pk[i] = pack_bf16(ex2(x0), ex2(x1));
+            add_bf16x2(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], pk[i]);
           }
           tmem_st16(tS + 16 * g, pk);
         }
-        l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+        l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         if (rescale) {
           // PV of the previous tile has completed (it was issued before this S)
 #pragma unroll 1
