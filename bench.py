@@ -192,16 +192,39 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def traffic_per_launch():
+def attend_bytes(shape: llsynth.Shape, resident_frames: int):
+    """Algorithmic DRAM bytes of one attend launch: q, the resident cache rows, the chunk's
+    k and v, and out (bf16)."""
+    row = shape.heads * shape.head_dim * 2
+    L = shape.chunk_tokens
+    return (3 * L + 2 * resident_frames * shape.tokens_per_frame + L) * row
+
+
+def traffic_record():
     """DRAM bytes per attend launch from the committed ncu summary, if it matches this source."""
-    p = os.path.join(ROOT, "profiles", "attend_tc_traffic.json")
+    p = os.path.join(ROOT, "profiles", "attend_tc_traffic.txt")
     if not os.path.exists(p):
         return None
+    rec = {}
     with open(p) as f:
-        d = json.load(f)
-    if d.get("source_hash") != kernel_source_hash():
+        for line in f:
+            if "=" in line and not line.lstrip().startswith("#"):
+                k, v = line.split("=", 1)
+                rec[k.strip()] = v.strip()
+    if rec.get("source_hash") != kernel_source_hash():
         return None
-    return d.get("dram_bytes_per_launch")
+    return rec
+
+
+def traffic_per_launch(alg_bytes_per_launch: float):
+    """Measured DRAM bytes per launch, scaled from the captured launch to this workload's
+    average launch by algorithmic bytes (the traffic grows with the keys read)."""
+    rec = traffic_record()
+    if rec is None:
+        return None, None
+    measured = float(rec["dram_bytes_per_launch"])
+    captured_alg = float(rec["algorithmic_bytes_per_launch"])
+    return measured * alg_bytes_per_launch / captured_alg, rec.get("workload")
 
 
 # ----------------------------------------------------------------------------
@@ -372,7 +395,11 @@ def run_ours(args, world, rank, local):
         "parallelism": "replicas x%d (independent streams, no collective)" % world}))
     result = base_result(args, world, step_frames * args.steps * world / (ms_max / 1e3), ms_max, config)
     roof = tensor_roofline("attend_tc_kernel<128>", step_flops * args.steps, n_att, ms_att, pk, pk_src)
-    roof["traffic"] = traffic_per_launch()
+    alg = sum(attend_bytes(shape, resident_count(S, W, t0)) for t0, _ in plan) / len(plan)
+    roof["algorithmic_bytes_per_launch"] = alg
+    roof["traffic"], src = traffic_per_launch(alg)
+    if src:
+        roof["traffic_source"] = "ncu capture of %s, scaled by algorithmic bytes" % src
     result.update({
         "tflops": step_flops * args.steps * world / (ms_max / 1e3) / 1e12,
         "roofline": roof,
@@ -432,7 +459,11 @@ def run_single(args, world, rank, local):
     result = base_result(args, world, C * args.steps * world / (ms_max / 1e3), ms_max, config)
     roof = tensor_roofline("attend_tc_kernel<128>", pass_flops * passes * args.steps, n_att, ms_att, pk, pk_src,
                            sustained=False)
-    roof["traffic"] = traffic_per_launch()
+    alg = attend_bytes(shape, S + W)
+    roof["algorithmic_bytes_per_launch"] = alg
+    roof["traffic"], src = traffic_per_launch(alg)
+    if src:
+        roof["traffic_source"] = "ncu capture of %s" % src
     result.update({
         "tflops": pass_flops * passes * args.steps * world / (ms_max / 1e3) / 1e12,
         "roofline": roof,

@@ -174,21 +174,6 @@ __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
-// D(tmem) (+)= A(smem) * B(smem)
-__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc));
-}
-// D(tmem) (+)= A(tmem) * B(smem)
-__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-      "r"(a), "l"(bdesc), "r"(idesc), "r"(acc));
-}
-
 #define LL_R8(i) "=r"(r[i + 0]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
                  "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
 #define LL_W8(i) "r"(r[i + 0]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \
@@ -258,11 +243,59 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
+// Eight (or four) MMAs of one group from a single asm block: k-step 0 accumulates
+// when acc != 0, the others always.  D(tmem) (+)= A(smem) * B(smem)
+__device__ __forceinline__ void mma8_ss(uint32_t d, const uint64_t (&a)[8], const uint64_t (&b)[8], uint32_t idesc,
+                                        uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\tsetp.ne.b32 p0, %18, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %1, p0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %1, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %1, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %1, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %1, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %1, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %1, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %17, %1, p1;\n\t}" ::"r"(d),
+      "r"(idesc), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]),
+      "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(acc));
+}
+__device__ __forceinline__ void mma4_ss(uint32_t d, const uint64_t (&a)[4], const uint64_t (&b)[4], uint32_t idesc,
+                                        uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\tsetp.ne.b32 p0, %10, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %1, p0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %1, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %1, p1;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %9, %1, p1;\n\t}" ::"r"(d),
+      "r"(idesc), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc));
+}
+// D(tmem) (+)= A(tmem: 8 k-steps of 8 columns from column a) * B(smem)
+__device__ __forceinline__ void mma8_ts(uint32_t d, uint32_t a, const uint64_t (&b)[8], uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b32 t;\n\tsetp.ne.b32 p0, %11, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %3, %1, p0;\n\t"
+      "add.u32 t, %2, 8;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [t], %4, %1, p1;\n\t"
+      "add.u32 t, %2, 16;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [t], %5, %1, p1;\n\t"
+      "add.u32 t, %2, 24;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [t], %6, %1, p1;\n\t"
+      "add.u32 t, %2, 32;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [t], %7, %1, p1;\n\t"
+      "add.u32 t, %2, 40;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [t], %8, %1, p1;\n\t"
+      "add.u32 t, %2, 48;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [t], %9, %1, p1;\n\t"
+      "add.u32 t, %2, 56;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [t], %10, %1, p1;\n\t}" ::"r"(d),
+      "r"(idesc), "r"(a), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
+      "r"(acc));
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
 // address, leading and stride byte offsets in 16-byte units, version 1).
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+__device__ __forceinline__ uint64_t make_desc(uint32_t lo, uint32_t hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+  return r;
 }
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M x N, A/B major-ness.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
@@ -473,21 +506,43 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       // ------------------------------ MMA issuer --------------------------------
       constexpr uint32_t kIdQK = idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
       constexpr uint32_t kIdPV = idesc_bf16(BM, D, 0, 1);   // P from TMEM; V is N(=d)-major
-      auto issue_qk = [&](int w, int stage) {
+      // The tensor core takes one 128x128x16 MMA per 64 clocks, but this thread
+      // shares its SMSP's issue slots with two busy softmax warps and gets few of
+      // them, so each MMA group must cost it as few instructions as possible:
+      // all operands are ready in registers and the eight MMAs of a group go out
+      // from one asm block.  The Q descriptors of both query tiles and the
+      // tensor-memory addresses of P are built once; the descriptors of a K or V
+      // tile differ from the ring's first stage only in the start address field
+      // of the low word (16-byte units; shared offsets stay below 256 KB, so no
+      // carry reaches the high word).
+      static_assert(D / 16 == 8 || D / 16 == 4, "k-steps per Q K^T group");
+      static_assert(BN / 16 == 8, "k-steps per P V group");
+      uint64_t dq[NQ][D / 16];
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (uint32_t)((ks >> 2) * kAtom + (ks & 3) * 32);
-          const uint64_t ad = sw128_desc(sQ + w * Cf::kQBytes + off, 16, 1024);
-          const uint64_t bd = sw128_desc(sKV + stage * Cf::kTileBytes + off, 16, 1024);
-          mma_ss(tmem + 256 + 128 * w, ad, bd, kIdQK, ks > 0 ? 1u : 0u);
-        }
+      for (int w = 0; w < NQ; ++w)
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          dq[w][ks] = sw128_desc(sQ + w * Cf::kQBytes + (ks >> 2) * kAtom + (ks & 3) * 32, 16, 1024);
+      const uint64_t dK0 = sw128_desc(sKV, 16, 1024);
+      const uint64_t dV0 = sw128_desc(sKV, kAtom, 1024);
+      const uint32_t k_lo0 = (uint32_t)dK0, k_hi = (uint32_t)(dK0 >> 32);
+      const uint32_t v_lo0 = (uint32_t)dV0, v_hi = (uint32_t)(dV0 >> 32);
+      auto issue_qk = [&](int w, int stage) {
+        const uint32_t lo = k_lo0 + (((uint32_t)stage * Cf::kTileBytes) >> 4);
+        uint64_t bd[D / 16];
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) bd[ks] = make_desc(lo + ((ks >> 2) * kAtom + (ks & 3) * 32) / 16, k_hi);
+        if constexpr (D / 16 == 8)
+          mma8_ss(tmem + 256 + 128 * w, dq[w], bd, kIdQK, 0u);
+        else
+          mma4_ss(tmem + 256 + 128 * w, dq[w], bd, kIdQK, 0u);
       };
       auto issue_pv = [&](int w, int stage, bool acc) {
+        const uint32_t lo = v_lo0 + (((uint32_t)stage * Cf::kTileBytes) >> 4);
+        uint64_t bd[BN / 16];
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-          const uint64_t bd = sw128_desc(sKV + stage * Cf::kTileBytes + ks * 16 * 128, kAtom, 1024);
-          mma_ts(tmem + 128 * w, tmem + 256 + 128 * w + ks * 8, bd, kIdPV, (acc || ks > 0) ? 1u : 0u);
-        }
+        for (int ks = 0; ks < BN / 16; ++ks) bd[ks] = make_desc(lo + (ks * 16 * 128) / 16, v_hi);
+        mma8_ts(tmem + 128 * w, tmem + 256 + 128 * w, bd, kIdPV, acc ? 1u : 0u);
       };
       Walker wk;
       walker_init(wk, p, blockIdx.x);
@@ -571,35 +626,25 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         ok = __all_sync(0xffffffffu, wait(bS, (jt + t) & 1, ctl));
         if (!ok) break;
         tc_fence_after();
-        // S in two halves: the max of the first 64 columns overlaps the load of the rest
+        // S: all four loads in flight, one wait
         uint32_t r[BN];
         tmem_ld32(tS + 0, r + 0);
         tmem_ld32(tS + 32, r + 32);
-        tmem_ld_wait();
-        reg_fence(r, BN / 2);
         tmem_ld32(tS + 64, r + 64);
         tmem_ld32(tS + 96, r + 96);
+        tmem_ld_wait();
+        reg_fence(r, BN);
         const int valid = j < nA ? a.La - j * BN : (a.mode == 1 ? row_end : a.Lb) - (j - nA) * BN;
-        if (valid < BN / 2) {
+        if (valid < BN) {
 #pragma unroll
-          for (int c = 0; c < BN / 2; ++c)
+          for (int c = 0; c < BN; ++c)
             if (c >= valid) r[c] = __float_as_uint(-INFINITY);
         }
         float mx[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) mx[i] = __uint_as_float(r[i]);
 #pragma unroll
-        for (int c = 4; c < BN / 2; c += 2)
-          mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
-        tmem_ld_wait();
-        reg_fence(r + BN / 2, BN / 2);
-        if (valid < BN) {
-#pragma unroll
-          for (int c = BN / 2; c < BN; ++c)
-            if (c >= valid) r[c] = __float_as_uint(-INFINITY);
-        }
-#pragma unroll
-        for (int c = BN / 2; c < BN; c += 2)
+        for (int c = 4; c < BN; c += 2)
           mx[(c >> 1) & 3] = max3f(mx[(c >> 1) & 3], __uint_as_float(r[c]), __uint_as_float(r[c + 1]));
         const float mt = max3f(max3f(mx[0], mx[1], mx[2]), mx[3], -INFINITY);
         const float m_new = fmaxf(m, mt * sl2);
