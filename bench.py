@@ -654,6 +654,8 @@ def run_reference(args, world, rank):
     step_frames = chunks * C
     step_flops = sum(attend_flops(L, lkv, H, d) for _, lkv in plan) * shape.layers
     budget = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    if args.ref_budget_s is not None:
+        budget = args.ref_budget_s
     for _ in range(args.warmup):
         oracle_rate(shape, budget_s=min(budget, 3.0))
     times, rates, threads, sample = [], [], 1, ""
@@ -683,6 +685,9 @@ def main():
     ap.add_argument("--workload", choices=["stream30", "single", "recache30", "sweep"], default="stream30",
                     help="stream30 (default: the 30-layer stack the metric names); the others time the "
                          "single-layer, prompt-switch recache and window/sink sweep workloads")
+    ap.add_argument("--ref-budget-s", type=float, default=None,
+                    help="seconds of oracle work per step of the reference arm (default: sized so the run takes "
+                         "about two minutes)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
