@@ -580,19 +580,24 @@ def run_sweep(args, world, rank, local):
 
 def run_e2e(ll, cache, shape, chunks, step_frames, world, rank, args):
     """Same stream through the public API with q/k/v copied in from pinned host memory and every
-    output copied back, double-buffered on copy streams."""
+    output copied back.  q, k and v go up on separate copy streams (several copy engines work
+    at once); `out` comes back on another; NB device buffer sets rotate so copies overlap the
+    attention of the previous layers."""
     H, d, T, C = shape.heads, shape.head_dim, shape.tokens_per_frame, shape.chunk_frames
     L = C * T
     pool = 4  # distinct pinned host input sets, cycled
+    NB = 3    # device buffer sets in flight
     host_in = [tuple(llsynth.seeded_normal(("bench-e2e", rank, i, t), (L, H, d)).pin_memory() for t in "qkv")
                for i in range(pool)]
-    host_out = [torch.empty((L, H, d), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    dev_in = [tuple(torch.empty((L, H, d), dtype=torch.bfloat16, device="cuda") for _ in range(3)) for _ in range(2)]
-    dev_out = [torch.empty((L, H, d), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    host_out = [torch.empty((L, H, d), dtype=torch.bfloat16).pin_memory() for _ in range(NB)]
+    dev_in = [tuple(torch.empty((L, H, d), dtype=torch.bfloat16, device="cuda") for _ in range(3)) for _ in range(NB)]
+    dev_out = [torch.empty((L, H, d), dtype=torch.bfloat16, device="cuda") for _ in range(NB)]
     comp = torch.cuda.current_stream()
-    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
-    done = [torch.cuda.Event() for _ in range(2)]
-    drained = [torch.cuda.Event() for _ in range(2)]
+    n_in = max(1, args.e2e_streams)
+    s_in = [torch.cuda.Stream() for _ in range(n_in)]
+    s_out = torch.cuda.Stream()
+    done = [torch.cuda.Event() for _ in range(NB)]     # attention of buffer set b finished
+    drained = [torch.cuda.Event() for _ in range(NB)]  # out of buffer set b copied back
     for e in done + drained:
         e.record(comp)
     bytes_in = bytes_out = 0
@@ -603,15 +608,19 @@ def run_e2e(ll, cache, shape, chunks, step_frames, world, rank, args):
         i = 0
         for c in range(chunks):
             for l in range(shape.layers):
-                b = i % 2
+                b = i % NB
                 src = host_in[i % pool]
-                s_in.wait_event(done[b])
-                with torch.cuda.stream(s_in):
-                    for dst, h in zip(dev_in[b], src):
+                ready = []
+                for ti, (dst, h) in enumerate(zip(dev_in[b], src)):
+                    st = s_in[ti % n_in]
+                    st.wait_event(done[b])
+                    with torch.cuda.stream(st):
                         dst.copy_(h, non_blocking=True)
-                ready = torch.cuda.Event()
-                ready.record(s_in)
-                comp.wait_event(ready)
+                    ev = torch.cuda.Event()
+                    ev.record(st)
+                    ready.append(ev)
+                for ev in ready:
+                    comp.wait_event(ev)
                 comp.wait_event(drained[b])
                 ll.ll_attend_chunk(cache, l, *dev_in[b], dev_out[b], True, comp)
                 done[b].record(comp)
@@ -637,8 +646,9 @@ def run_e2e(ll, cache, shape, chunks, step_frames, world, rank, args):
     barrier(world)
     return {"value": step_frames * steps * world / el, "unit": UNIT, "steps": steps,
             "h2d_bytes_per_step": bytes_in // steps, "d2h_bytes_per_step": bytes_out // steps,
-            "how": "pinned host q/k/v -> device (copy stream) -> ll_attend_chunk -> out -> pinned host "
-                   "(copy stream), double-buffered; wall clock"}
+            "h2d_GBps": bytes_in / el / 1e9, "d2h_GBps": bytes_out / el / 1e9,
+            "how": "pinned host q/k/v -> device (%d copy stream%s) -> ll_attend_chunk -> out -> pinned host "
+                   "(copy stream), %d buffer sets in flight; wall clock" % (n_in, "s" if n_in > 1 else "", NB)}
 
 
 # ----------------------------------------------------------------------------
@@ -689,6 +699,7 @@ def main():
                     help="seconds of oracle work per step of the reference arm (default: sized so the run takes "
                          "about two minutes)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-streams", type=int, default=3, help="host-to-device copy streams of the e2e measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
