@@ -41,6 +41,16 @@ Readings taken where the pages are silent (each is listed in the design doc):
   unchanged.  The optional prefill attention of a recache is block-causal over
   that list in blocks of C frames.
 
+Two other readings are kept as options, because the pages leave them open:
+
+* ``chunk_mask="frame"``: the model is called frame-level autoregressive, so a
+  query of chunk frame t0 + i may instead see only the chunk's frames t0 .. t0 + i
+  (plus every cached frame); the recache prefill then uses blocks of one frame.
+* ``recache_scope="window"``: §3.3 says the recache rebuilds the cache only from
+  the most recent W frames, so the sink may instead keep its K/V; only the window
+  frames are rewritten, and the prefill queries of the window frames see the
+  (unchanged) sink plus the fresh window, block-causal over the window.
+
 Parity pins: every function here is pinned by tests under ``tests/`` that do
 not call back into this module's own formulas (brute force, closed forms,
 library routines, invariants, hand-written golden tables).
@@ -162,6 +172,25 @@ def block_causal_visible(T: int, C: int, Lkv: int):
     return visible
 
 
+def prefix_then_block_causal_visible(n_prefix: int, block_tokens: int, Lkv: int):
+    """Key mask with a fully visible prefix, then block causality over the rest.
+
+    Keys [0, n_prefix) (cached frames) are seen by every query; key j >= n_prefix
+    is seen by query row qi iff (j - n_prefix) // block_tokens <= qi // block_tokens.
+    With one-frame blocks this is the frame-causal chunk of the "frame-level
+    autoregressive" reading; with C-frame blocks after a sink prefix it is the
+    keep-sink recache prefill.
+    """
+    kj = np.arange(Lkv)
+    after = kj >= n_prefix
+    key_block = np.where(after, (kj - n_prefix) // block_tokens, -1)
+
+    def visible(qi: int) -> np.ndarray:
+        return ~after | (key_block <= (qi // block_tokens))
+
+    return visible
+
+
 # ---------------------------------------------------------------------------
 # The cache (one per layer) and the calls of the hot path
 # ---------------------------------------------------------------------------
@@ -179,7 +208,8 @@ class OracleCache:
     """Per-layer rolling KV cache with a frame sink, kept as explicit frame lists."""
 
     def __init__(self, layers: int, heads: int, head_dim: int, tokens_per_frame: int,
-                 sink_frames: int, window_frames: int, chunk_frames: int):
+                 sink_frames: int, window_frames: int, chunk_frames: int,
+                 chunk_mask: str = "chunk", recache_scope: str = "resident"):
         if min(layers, heads, head_dim, tokens_per_frame, chunk_frames) < 1:
             raise ValueError("layers, heads, head_dim, tokens_per_frame, chunk_frames must be >= 1")
         if sink_frames < 0 or window_frames < 0:
@@ -187,6 +217,24 @@ class OracleCache:
         self.L, self.H, self.d = layers, heads, head_dim
         self.T, self.S, self.W, self.C = tokens_per_frame, sink_frames, window_frames, chunk_frames
         self.layers = [OracleLayer() for _ in range(layers)]
+        self.set_chunk_mask(chunk_mask)
+        self.set_recache_scope(recache_scope)
+
+    def set_chunk_mask(self, mode: str) -> None:
+        """"chunk" (default): a chunk sees all of its frames; "frame": only its frames up to the query's."""
+        if mode not in ("chunk", "frame"):
+            raise ValueError(mode)
+        self.chunk_mask = mode
+
+    def set_recache_scope(self, scope: str) -> None:
+        """"resident" (default): recache rewrites sink and window; "window": the sink keeps its K/V."""
+        if scope not in ("resident", "window"):
+            raise ValueError(scope)
+        self.recache_scope = scope
+
+    def _block_frames(self) -> int:
+        """Frames per causal block of the chunk / prefill masks."""
+        return 1 if self.chunk_mask == "frame" else self.C
 
     # -- state ---------------------------------------------------------------
     def state(self, layer: int) -> tuple[int, list[int]]:
@@ -218,7 +266,10 @@ class OracleCache:
         past = resident_frames(self.S, self.W, t0)
         K = np.concatenate([lay.frames[f][0] for f in past] + [k], axis=0)
         V = np.concatenate([lay.frames[f][1] for f in past] + [v], axis=0)
-        out = masked_attention(q, K, V, visible=None, rows=rows)
+        visible = None
+        if self.chunk_mask == "frame":
+            visible = prefix_then_block_causal_visible(len(past) * T, T, K.shape[0])
+        out = masked_attention(q, K, V, visible=visible, rows=rows)
         if commit:
             self._commit(layer, k, v)
         return out
@@ -247,14 +298,22 @@ class OracleCache:
             if f not in keep:
                 del lay.frames[f]
 
-    def recache(self, layer: int, k_win, v_win) -> None:
-        """§3.1 "KV recache": replace the K/V of the R resident frames in list order.
+    def recache_frames(self, layer: int) -> list[int]:
+        """Frames a recache rewrites, in the order of k_win / v_win."""
+        n = self.layers[layer].n
+        if self.recache_scope == "window":
+            return window_frames(self.S, self.W, n)
+        return resident_frames(self.S, self.W, n)
 
-        k_win, v_win: [R*T, H, d] for frames [sink asc, window asc].  Frame indices
-        and the committed count do not change.
+    def recache(self, layer: int, k_win, v_win) -> None:
+        """§3.1 "KV recache": replace the K/V of the recached frames in list order.
+
+        k_win, v_win: [R*T, H, d] for frames [sink asc, window asc] (scope
+        "resident") or [window asc] (scope "window").  Frame indices and the
+        committed count do not change.
         """
         lay = self.layers[layer]
-        frames = resident_frames(self.S, self.W, lay.n)
+        frames = self.recache_frames(layer)
         if not frames:
             raise ValueError("recache of an empty layer")
         T = self.T
@@ -265,23 +324,34 @@ class OracleCache:
             lay.frames[f] = (k_win[i * T:(i + 1) * T], v_win[i * T:(i + 1) * T])
 
     def recache_attend(self, layer: int, q_win, k_win, v_win, rows=None) -> np.ndarray:
-        """Recache with the prefill attention: block-causal over the resident list.
+        """Recache with the prefill attention: block-causal over the recached list.
 
-        The list [sink asc, window asc] is cut into blocks of C frames; query
-        rows in block g see key blocks 0..g.  The fresh K/V then replace the
-        resident frames as in :meth:`recache`.
+        Scope "resident": the list [sink asc, window asc] is cut into blocks of C
+        frames (one frame with the frame mask); query rows in block g see key
+        blocks 0..g.  Scope "window": the queries are the window frames'; they
+        see every sink frame (its cached K/V) plus the fresh window, block-causal
+        over the window.  The fresh K/V then replace the recached frames as in
+        :meth:`recache`.
         """
         lay = self.layers[layer]
-        R = len(resident_frames(self.S, self.W, lay.n))
+        R = len(self.recache_frames(layer))
         if R == 0:
             raise ValueError("recache of an empty layer")
         q_win = np.asarray(q_win, dtype=np.float64)
         k_win = np.asarray(k_win, dtype=np.float64)
         v_win = np.asarray(v_win, dtype=np.float64)
-        L = R * self.T
+        T = self.T
+        L = R * T
         assert q_win.shape == (L, self.H, self.d)
-        out = masked_attention(q_win, k_win, v_win,
-                               visible=block_causal_visible(self.T, self.C, L), rows=rows)
+        block = self._block_frames() * T
+        if self.recache_scope == "window":
+            sink = sink_frames(self.S, lay.n)
+            K = np.concatenate([lay.frames[f][0] for f in sink] + [k_win], axis=0)
+            V = np.concatenate([lay.frames[f][1] for f in sink] + [v_win], axis=0)
+            visible = prefix_then_block_causal_visible(len(sink) * T, block, K.shape[0])
+            out = masked_attention(q_win, K, V, visible=visible, rows=rows)
+        else:
+            out = masked_attention(q_win, k_win, v_win, visible=block_causal_visible(block, 1, L), rows=rows)
         self.recache(layer, k_win, v_win)
         return out
 
