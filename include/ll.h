@@ -107,7 +107,9 @@ LL_API ll_status ll_attend_chunk(ll_cache* cache, int layer, const void* q, cons
  * in `layer` (R = min(S,n) + min(W, max(0, n - S)), n = frames committed) by
  * k_win/v_win, [R*T][H][d], given in list order (sink frames ascending, then
  * window frames ascending).  Frame indices and n do not change.
- * Returns LL_ERR_STATE if the layer is empty (n = 0).
+ * Returns LL_ERR_STATE if the layer is empty (n = 0).  With
+ * ll_set_recache_scope(LL_RECACHE_WINDOW) only the window frames are given
+ * and rewritten.
  */
 LL_API ll_status ll_recache(ll_cache* cache, int layer, const void* k_win, const void* v_win,
                      void* stream);
@@ -128,6 +130,32 @@ LL_API ll_status ll_recache_attend(ll_cache* cache, int layer, const void* q_win
  * which passes 1e-2 once |o| >= 4).  LL_BF16 on an fp32 cache is rejected.
  */
 LL_API ll_status ll_set_output_dtype(ll_cache* cache, ll_dtype dtype);
+
+/*
+ * Options for two readings the pages leave open; both default to the first value.
+ *
+ * ll_set_chunk_mask -- which of the chunk's own keys a query sees.
+ *   LL_MASK_CHUNK: all of them (chunk-level block causality; the default).
+ *   LL_MASK_FRAME: the model is called "frame-level autoregressive", so a query
+ *     of chunk frame t0 + i sees the cached frames and the chunk's frames
+ *     t0 .. t0 + i only; the recache prefill then uses one-frame blocks.
+ * Applies to later ll_attend_chunk / ll_recache_attend calls of this cache.
+ */
+typedef enum { LL_MASK_CHUNK = 0, LL_MASK_FRAME = 1 } ll_chunk_mask;
+LL_API ll_status ll_set_chunk_mask(ll_cache* cache, int mode);
+
+/*
+ * ll_set_recache_scope -- which frames a recache rewrites.
+ *   LL_RECACHE_RESIDENT: every resident frame, sink and window (the default).
+ *   LL_RECACHE_WINDOW: §3.3 "rebuild the cache only from the most recent W
+ *     frames": the sink keeps its K/V; k_win / v_win (and q_win, out_win) hold
+ *     the Rw = min(W, max(0, n - S)) window frames, ascending; the prefill
+ *     queries see every cached sink frame plus the fresh window, block-causal
+ *     over the window list from its first frame.  A recache with no window
+ *     frame resident returns LL_ERR_STATE.
+ */
+typedef enum { LL_RECACHE_RESIDENT = 0, LL_RECACHE_WINDOW = 1 } ll_recache_scope;
+LL_API ll_status ll_set_recache_scope(ll_cache* cache, int scope);
 
 /* §4.4 Table 4 ("no KV cache"): drop every frame of every layer (metadata only). */
 LL_API ll_status ll_reset(ll_cache* cache);

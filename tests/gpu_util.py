@@ -99,6 +99,13 @@ class Lockstep:
                 self.host[layer][t0 + i] = (kc[i * self.T:(i + 1) * self.T], vc[i * self.T:(i + 1) * self.T])
         return out
 
+    def set_options(self, chunk_mask="chunk", recache_scope="resident"):
+        """The two optional readings, on the library cache and on the oracle alike."""
+        self.ll.ll_set_chunk_mask(self.cache, chunk_mask)
+        self.ll.ll_set_recache_scope(self.cache, recache_scope)
+        self.orc.set_chunk_mask(chunk_mask)
+        self.orc.set_recache_scope(recache_scope)
+
     def commit_placeholder(self, layer, q, k, v):
         """GPU gets the real chunk; the oracle a zero chunk.
 
@@ -133,7 +140,7 @@ class Lockstep:
         if not self.keep:
             return
         kc, vc = k_win.cpu(), v_win.cpu()
-        for i, f in enumerate(self.orc.resident(layer)):
+        for i, f in enumerate(self.orc.recache_frames(layer)):
             self.host[layer][f] = (kc[i * self.T:(i + 1) * self.T], vc[i * self.T:(i + 1) * self.T])
 
     def check_state(self, layers=None):

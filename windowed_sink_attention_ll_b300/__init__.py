@@ -36,8 +36,11 @@ EXPORTS = ("ll_status_str", "ll_cache_create", "ll_cache_destroy", "ll_attend_ch
            "ll_recache_attend", "ll_reset", "ll_cache_state", "ll_cache_read", "ll_sync",
            "ll_cache_info", "ll_frame_slot", "ll_resident_frames", "ll_launch_count",
            "ll_debug_inject_stall", "ll_debug_use_simt", "ll_profile_enable", "ll_profile_read",
-           "ll_set_output_dtype", "ll_debug_attend_schedule", "ll_attend_chunk_noalloc")
+           "ll_set_output_dtype", "ll_debug_attend_schedule", "ll_attend_chunk_noalloc",
+           "ll_set_chunk_mask", "ll_set_recache_scope")
 LL_KERNEL_ATTEND, LL_KERNEL_PREFILL, LL_KERNEL_COPY = 0, 1, 2
+LL_MASK_CHUNK, LL_MASK_FRAME = 0, 1
+LL_RECACHE_RESIDENT, LL_RECACHE_WINDOW = 0, 1
 
 
 class LLError(RuntimeError):
@@ -83,6 +86,8 @@ def _lib() -> ctypes.CDLL:
                                                ctypes.POINTER(i32)]),
             "ll_profile_read": (i32, [vp, i32, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]),
             "ll_attend_chunk_noalloc": (i32, [vp, vp, vp, i32, i64, vp, vp, i32, vp, i32, i32, vp, vp]),
+            "ll_set_chunk_mask": (i32, [vp, i32]),
+            "ll_set_recache_scope": (i32, [vp, i32]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -286,6 +291,20 @@ def ll_set_output_dtype(cache: LLCache, dtype) -> None:
         dtype = LL_BF16 if dtype == torch.bfloat16 else LL_FP32 if dtype == torch.float32 else -1
     _check(_lib().ll_set_output_dtype(cache.ptr, dtype), "ll_set_output_dtype")
     cache.out_dtype = torch.float32 if dtype == LL_FP32 else torch.bfloat16
+
+
+def ll_set_chunk_mask(cache: LLCache, mode) -> None:
+    """LL_MASK_CHUNK / "chunk" (default) or LL_MASK_FRAME / "frame" (see include/ll.h)."""
+    mode = {"chunk": LL_MASK_CHUNK, "frame": LL_MASK_FRAME}.get(mode, mode)
+    _check(_lib().ll_set_chunk_mask(cache.ptr, mode), "ll_set_chunk_mask")
+    cache.chunk_mask = mode
+
+
+def ll_set_recache_scope(cache: LLCache, scope) -> None:
+    """LL_RECACHE_RESIDENT / "resident" (default) or LL_RECACHE_WINDOW / "window" (see include/ll.h)."""
+    scope = {"resident": LL_RECACHE_RESIDENT, "window": LL_RECACHE_WINDOW}.get(scope, scope)
+    _check(_lib().ll_set_recache_scope(cache.ptr, scope), "ll_set_recache_scope")
+    cache.recache_scope = scope
 
 
 def ll_debug_attend_schedule(Lq: int, La: int, Lb: int, heads: int, max_ctas: int):

@@ -5,7 +5,8 @@
 // "LongLive", §3.3 "Frame sink" / "Short window attention": each query of the
 // chunk attends to [resident sink + window frames of the cache || the chunk's
 // own K/V]; in prefill mode (§3.1 "KV recache") it attends block-causally over
-// the recache window.  The key/value list is read from the two sources that
+// the recache window, and in mode 2 it sees every cached key and the chunk's
+// own keys block-causally.  The key/value list is read from the two sources that
 // AttendArgs describes; the order of keys does not change the softmax.
 #include <cuda_bf16.h>
 
@@ -72,7 +73,7 @@ __global__ void __launch_bounds__(kWarps * 32) attend_simt_kernel(const __grid_c
   for (int j = 0; j < a.La; ++j) visit(kc + (int64_t)j * D, vc + (int64_t)j * D);
   // source B: caller tensor rows, all of them (attend) or a block-causal prefix (prefill)
   int end = a.Lb;
-  if (a.mode == 1) {
+  if (a.mode != 0) {
     const int64_t e = ((int64_t)row / a.block_tokens + 1) * a.block_tokens;
     end = e < a.Lb ? (int)e : a.Lb;
   }

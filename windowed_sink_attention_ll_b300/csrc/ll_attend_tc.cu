@@ -11,7 +11,9 @@
 // so the kernel walks the resident cache rows in slot order (one contiguous
 // run per head, see ll_host.cu) and then the chunk's rows.  In prefill mode
 // (§3.1 "KV recache") there is one source, the recache window, and query row
-// i sees key j iff j / block_tokens <= i / block_tokens.
+// i sees key j iff j / block_tokens <= i / block_tokens.  Mode 2 keeps the
+// attend schedule and every cached key, and masks the chunk's own keys the
+// same block-causal way (the frame-causal chunk and the keep-sink prefill).
 //
 // CTA = one head x 256 query rows (two 128-row tiles that share every K/V
 // tile).  Attend launches are persistent: whole rounds of items, then the
@@ -387,7 +389,7 @@ __host__ __device__ __forceinline__ bool walker_next(Walker& w, const TcParams& 
 
 // head, first query row and cache-tile count of an item
 __device__ __forceinline__ void item_geom(const TcParams& p, int item, int& head, int& q0, int& nA) {
-  if (p.a.mode == 0) {
+  if (p.a.mode != 1) {
     head = item / p.nqb;
     q0 = (item - head * p.nqb) * NQ * BM;
     nA = (p.a.La + BN - 1) / BN;
@@ -615,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       item_geom(p, pc.item, head, q0, nA);
       const int qrow = q0 + w * BM + row;
       int row_end = a.Lb;
-      if (a.mode == 1) {
+      if (a.mode != 0) {
         const long long e = ((long long)qrow / a.block_tokens + 1) * a.block_tokens;
         row_end = (int)(e < a.Lb ? e : a.Lb);
       }
@@ -634,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         tmem_ld32(tS + 96, r + 96);
         tmem_ld_wait();
         reg_fence(r, BN);
-        const int valid = j < nA ? a.La - j * BN : (a.mode == 1 ? row_end : a.Lb) - (j - nA) * BN;
+        const int valid = j < nA ? a.La - j * BN : (a.mode != 0 ? row_end : a.Lb) - (j - nA) * BN;
         if (valid < BN) {
 #pragma unroll
           for (int c = 0; c < BN; ++c)

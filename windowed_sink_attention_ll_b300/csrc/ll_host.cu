@@ -44,7 +44,9 @@ struct ll_cache {
   int stall_inject = 0;
   int stall_timeout_us = 0;
   int use_simt = 0;
-  int out_f32 = 0;  // outputs in fp32 on a bf16 cache
+  int out_f32 = 0;        // outputs in fp32 on a bf16 cache
+  int chunk_mask = LL_MASK_CHUNK;
+  int recache_scope = LL_RECACHE_RESIDENT;
   // per-kernel timing (ll_profile_enable / ll_profile_read)
   struct Mark {
     int kind;
@@ -331,6 +333,11 @@ ll_status ll_attend_chunk(ll_cache* c, int layer, const void* q, const void* k, 
   a.Lq = c->C * c->T;
   a.mode = 0;
   a.block_tokens = c->C * c->T;
+  if (c->chunk_mask == LL_MASK_FRAME && c->C > 1) {
+    // frame-causal chunk: cached keys all visible, the chunk's own keys up to the query's frame
+    a.mode = 2;
+    a.block_tokens = c->T;
+  }
   if (ll_status s = launch_attend(c, a, st)) return s;
   if (!commit) return LL_OK;
 
@@ -361,7 +368,13 @@ static ll_status recache_common(ll_cache* c, int layer, const void* q_win, const
   if (q_win && (out_win == q_win || out_win == k_win || out_win == v_win)) return LL_ERR_INVALID_ARG;
   const int64_t n = c->n[layer];
   std::vector<int64_t> frames(c->S + c->W + 1);
-  const int R = ll_resident_frames(c->S, c->W, n, frames.data());
+  int R = ll_resident_frames(c->S, c->W, n, frames.data());
+  const int sink = (int)(n < c->S ? n : c->S);  // resident sink frames: the first `sink` of the list
+  if (c->recache_scope == LL_RECACHE_WINDOW) {
+    // keep-sink scope: only the window frames are rewritten
+    frames.erase(frames.begin(), frames.begin() + sink);
+    R -= sink;
+  }
   if (R == 0) return LL_ERR_STATE;
   if (ll_status s = take_device_error(c)) return s;
   if (ll_status s = set_device(c)) return s;
@@ -370,13 +383,19 @@ static ll_status recache_common(ll_cache* c, int layer, const void* q_win, const
     ll::AttendArgs a = base_args(c, layer);
     a.q = q_win;
     a.out = out_win;
-    a.La = 0;
     a.kn = k_win;
     a.vn = v_win;
     a.Lb = R * c->T;
     a.Lq = R * c->T;
-    a.mode = 1;
-    a.block_tokens = c->C * c->T;
+    a.block_tokens = (c->chunk_mask == LL_MASK_FRAME ? 1 : c->C) * c->T;
+    if (c->recache_scope == LL_RECACHE_WINDOW) {
+      // window queries see the cached sink rows (slots [0, sink)) and the fresh window
+      a.La = sink * c->T;
+      a.mode = 2;
+    } else {
+      a.La = 0;
+      a.mode = 1;
+    }
     if (ll_status s = launch_attend(c, a, st)) return s;
   }
   std::vector<int> slot_of(R);
@@ -403,6 +422,18 @@ ll_status ll_set_output_dtype(ll_cache* c, ll_dtype dtype) {
   } else {
     return LL_ERR_INVALID_ARG;
   }
+  return LL_OK;
+}
+
+ll_status ll_set_chunk_mask(ll_cache* c, int mode) {
+  if (!c || (mode != LL_MASK_CHUNK && mode != LL_MASK_FRAME)) return LL_ERR_INVALID_ARG;
+  c->chunk_mask = mode;
+  return LL_OK;
+}
+
+ll_status ll_set_recache_scope(ll_cache* c, int scope) {
+  if (!c || (scope != LL_RECACHE_RESIDENT && scope != LL_RECACHE_WINDOW)) return LL_ERR_INVALID_ARG;
+  c->recache_scope = scope;
   return LL_OK;
 }
 

@@ -42,6 +42,8 @@ cudaError_t launch_copy_frames(const CopyFramesArgs& a, cudaStream_t stream);
 // mode 0 (attend): every query sees all La + Lb keys.
 // mode 1 (prefill): La = 0 and query row i sees keys j of source B with
 //             j / block_tokens <= i / block_tokens.
+// mode 2 (masked attend): every key of source A, and keys j of source B with
+//             j / block_tokens <= i / block_tokens (attend schedule).
 // ---------------------------------------------------------------------------
 struct AttendArgs {
   const void* q;      // [Lq][H][d]
