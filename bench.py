@@ -69,6 +69,46 @@ def attend_flops(Lq, Lkv, H, d):
     return 4.0 * Lq * Lkv * H * d
 
 
+def masked_pairs(Lq, La, Lb, block):
+    """Query-key pairs an attention visits: every row sees La cached keys plus, of the Lb
+    fresh keys, all of them (block None) or the blocks up to its own (block-causal)."""
+    if block is None:
+        return Lq * (La + Lb)
+    total = Lq * La
+    for g0 in range(0, Lq, block):
+        total += min(block, Lq - g0) * min(Lb, g0 + block)
+    return total
+
+
+def chunk_pairs(shape, t0, chunk_mask):
+    """Pairs of one chunk attend at frame t0 (frame mask: the chunk's keys in frame blocks)."""
+    T, C = shape.tokens_per_frame, shape.chunk_frames
+    L = C * T
+    La = resident_count(shape.sink_frames, shape.window_frames, t0) * T
+    return masked_pairs(L, La, L, T if (chunk_mask == "frame" and C > 1) else None)
+
+
+def prefill_pairs(shape, n, chunk_mask, recache_scope):
+    """Pairs of one recache prefill after n committed frames."""
+    T, C, S, W = shape.tokens_per_frame, shape.chunk_frames, shape.sink_frames, shape.window_frames
+    block = (1 if chunk_mask == "frame" else C) * T
+    sink = min(S, n)
+    win = min(W, max(0, n - S))
+    if recache_scope == "window":
+        return masked_pairs(win * T, sink * T, win * T, block)
+    R = (sink + win) * T
+    return masked_pairs(R, 0, R, block)
+
+
+def pair_flops(pairs, H, d):
+    return 4.0 * pairs * H * d
+
+
+def set_options(ll, cache, args):
+    ll.ll_set_chunk_mask(cache, args.chunk_mask)
+    ll.ll_set_recache_scope(cache, args.recache_scope)
+
+
 def append_bytes(shape: llsynth.Shape, frames_written: int):
     """K and V: read from the chunk tensors and written to the cache, per committed frame."""
     return 2 * 2 * frames_written * shape.tokens_per_frame * shape.heads * shape.head_dim * 2
@@ -364,7 +404,7 @@ def run_ours(args, world, rank, local):
     L = C * T
     plan = stream_plan(shape, chunks)
     step_frames = chunks * C
-    step_flops = sum(attend_flops(L, lkv, H, d) for _, lkv in plan) * shape.layers
+    step_flops = sum(pair_flops(chunk_pairs(shape, t0, args.chunk_mask), H, d) for t0, _ in plan) * shape.layers
     step_append = sum(append_bytes(shape, frames_written(shape, t0)) for t0, _ in plan) * shape.layers
 
     # inputs: independent seeded q/k/v per (rank, layer, chunk), resident before timing
@@ -372,6 +412,7 @@ def run_ours(args, world, rank, local):
                for c in range(chunks)] for l in range(shape.layers)]
     outs = [torch.empty((L, H, d), dtype=torch.bfloat16, device="cuda") for _ in range(shape.layers)]
     cache = ll.ll_cache_create(shape.layers, H, d, T, S, W, C, ll.LL_BF16)
+    set_options(ll, cache, args)
     stream = torch.cuda.current_stream()
 
     def step():
@@ -392,6 +433,7 @@ def run_ours(args, world, rank, local):
         "chunks": chunks,
         "l2": "inputs larger than L2 (%.1f GB q/k/v + %.2f GB cache per rank)" % (
             3 * L * H * d * 2 * chunks * shape.layers / 1e9, 2 * shape.layers * (S + W) * T * H * d * 2 / 1e9),
+        "chunk_mask": args.chunk_mask, "recache_scope": args.recache_scope,
         "parallelism": "replicas x%d (independent streams, no collective)" % world}))
     result = base_result(args, world, step_frames * args.steps * world / (ms_max / 1e3), ms_max, config)
     roof = tensor_roofline("attend_tc_kernel<128>", step_flops * args.steps, n_att, ms_att, pk, pk_src)
@@ -429,6 +471,7 @@ def run_single(args, world, rank, local):
     L = C * T
     passes = llsynth.SINGLE_LAYER_PASSES
     cache = ll.ll_cache_create(1, H, d, T, S, W, C, ll.LL_BF16)
+    set_options(ll, cache, args)
     for c in range((S + W) // C):
         q, k, v = (llsynth.seeded_normal(("bench-single-fill", rank, c, t), (L, H, d), device="cuda",
                                          per_head_scale=True) for t in "qkv")
@@ -438,8 +481,7 @@ def run_single(args, world, rank, local):
                                            per_head_scale=True) for t in "qkv") for p in range(passes)]
               for i in range(pool)]
     out = torch.empty((L, H, d), dtype=torch.bfloat16, device="cuda")
-    lkv = (S + W + C) * T
-    pass_flops = attend_flops(L, lkv, H, d)
+    pass_flops = pair_flops(chunk_pairs(shape, S + W, args.chunk_mask), H, d)
     it = [0]
 
     def step():
@@ -455,7 +497,8 @@ def run_single(args, world, rank, local):
     pk, pk_src = peaks()
     config = {"workload": "single: 1 Wan-shaped layer at steady state, H=12, d=128, T=1560, C=3, S=3, W=9, "
                           "Lkv=23400, 4 passes per chunk (commit on the last), per-head scales 0.5-2.0"}
-    config.update(shape_config(shape, {"passes": passes, "l2": "8 distinct chunks cycled (1.4 GB of q/k/v)"}))
+    config.update(shape_config(shape, {"passes": passes, "l2": "8 distinct chunks cycled (1.4 GB of q/k/v)",
+                                       "chunk_mask": args.chunk_mask}))
     result = base_result(args, world, C * args.steps * world / (ms_max / 1e3), ms_max, config)
     roof = tensor_roofline("attend_tc_kernel<128>", pass_flops * passes * args.steps, n_att, ms_att, pk, pk_src,
                            sustained=False)
@@ -484,7 +527,7 @@ def run_recache30(args, world, rank, local):
     H, d, T, S, W, C = (shape.heads, shape.head_dim, shape.tokens_per_frame, shape.sink_frames,
                         shape.window_frames, shape.chunk_frames)
     L = C * T
-    R = S + W
+    R = W if args.recache_scope == "window" else S + W  # frames a recache rewrites at a switch
     pool = 20  # chunk inputs cycled per layer (26 GB in total: far beyond L2)
     inputs = [[tuple(llsynth.seeded_normal(("bench-rc", rank, l, c, t), (L, H, d), device="cuda") for t in "qkv")
                for c in range(pool)] for l in range(shape.layers)]
@@ -494,12 +537,13 @@ def run_recache30(args, world, rank, local):
     outs = [torch.empty((L, H, d), dtype=torch.bfloat16, device="cuda") for _ in range(shape.layers)]
     out_rc = torch.empty((R * T, H, d), dtype=torch.bfloat16, device="cuda")
     cache = ll.ll_cache_create(shape.layers, H, d, T, S, W, C, ll.LL_BF16)
+    set_options(ll, cache, args)
     stream = torch.cuda.current_stream()
     plan = stream_plan(shape, chunks)
-    att_flops = sum(attend_flops(L, lkv, H, d) for _, lkv in plan) * shape.layers
-    # block-causal prefill over R frames in blocks of C frames: block g sees blocks 0..g
-    nb = R // C
-    pre_flops = 4.0 * (C * T) ** 2 * (nb * (nb + 1) // 2) * H * d
+    att_flops = sum(pair_flops(chunk_pairs(shape, t0, args.chunk_mask), H, d) for t0, _ in plan) * shape.layers
+    # block-causal prefill (blocks of C frames, or of one frame with the frame mask); the
+    # switches come after at least S + W frames, so the prefill shape is the same at each
+    pre_flops = pair_flops(prefill_pairs(shape, S + W, args.chunk_mask, args.recache_scope), H, d)
     switches = len(llsynth.RECACHE30_SWITCHES)
     step_pre_flops = pre_flops * shape.layers * switches
 
@@ -521,7 +565,8 @@ def run_recache30(args, world, rank, local):
     config = {"workload": "recache30: 30 layers x 40 chunks (120 latent frames), recache prefill of 12 frames "
                           "(18720 tokens, block-causal in 3-frame blocks) in every layer before chunks 10, 20, 30"}
     config.update(shape_config(shape, {"chunks": chunks, "switches": list(llsynth.RECACHE30_SWITCHES),
-                                       "l2": "inputs larger than L2 (41 GB per rank)"}))
+                                       "l2": "inputs larger than L2 (41 GB per rank)",
+                                       "chunk_mask": args.chunk_mask, "recache_scope": args.recache_scope}))
     result = base_result(args, world, chunks * C * args.steps * world / (ms_max / 1e3), ms_max, config)
     result.update({
         "tflops": (att_flops + step_pre_flops) * args.steps * world / (ms_max / 1e3) / 1e12,
@@ -551,6 +596,7 @@ def run_sweep(args, world, rank, local):
     for W in llsynth.SWEEP_W:
         for S in llsynth.SWEEP_S:
             cache = ll.ll_cache_create(1, H, d, T, S, W, C, ll.LL_BF16)
+            set_options(ll, cache, args)
             while ll.ll_cache_state(cache, 0)[0] < S + W + C:  # steady state: sink and window full
                 ll.ll_attend_chunk(cache, 0, *inputs[0], out, True)
             lkv = (S + W + C) * T
@@ -563,7 +609,8 @@ def run_sweep(args, world, rank, local):
 
             ms, clocks, launches, prof = timed_region(args, world, local, [cache], step)
             n_att, ms_att = prof[ll.LL_KERNEL_ATTEND]
-            flops = attend_flops(L, lkv, H, d) * 10 * args.steps
+            flops = pair_flops(chunk_pairs(llsynth.Shape(1, H, d, T, S, W, C), S + W, args.chunk_mask), H, d) \
+                * 10 * args.steps
             rows.append({"W": W, "S": S, "Lkv": lkv, "ms_per_chunk": ms / (10 * args.steps),
                          "attend_tflops": flops / (ms_att / 1e3) / 1e12,
                          "attend_frac_of_burst": flops / (ms_att / 1e3) / 1e12 / pk.get("bf16_tflops", 1800.0)})
@@ -695,6 +742,10 @@ def main():
     ap.add_argument("--workload", choices=["stream30", "single", "recache30", "sweep"], default="stream30",
                     help="stream30 (default: the 30-layer stack the metric names); the others time the "
                          "single-layer, prompt-switch recache and window/sink sweep workloads")
+    ap.add_argument("--chunk-mask", choices=["chunk", "frame"], default="chunk",
+                    help="chunk (default): a chunk sees all its frames; frame: the frame-causal reading")
+    ap.add_argument("--recache-scope", choices=["resident", "window"], default="resident",
+                    help="resident (default): recache rewrites sink and window; window: the sink keeps its K/V")
     ap.add_argument("--ref-budget-s", type=float, default=None,
                     help="seconds of oracle work per step of the reference arm (default: sized so the run takes "
                          "about two minutes)")

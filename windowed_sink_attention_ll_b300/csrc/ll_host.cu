@@ -137,8 +137,9 @@ struct ProfileScope {
   }
 };
 
-ll_status launch_attend(ll_cache* c, const ll::AttendArgs& a, cudaStream_t st) {
-  ProfileScope prof(c, st, a.mode == 1 ? LL_KERNEL_PREFILL : LL_KERNEL_ATTEND);
+// kind: LL_KERNEL_ATTEND (chunk attention) or LL_KERNEL_PREFILL (recache prefill)
+ll_status launch_attend(ll_cache* c, const ll::AttendArgs& a, cudaStream_t st, int kind) {
+  ProfileScope prof(c, st, kind);
   cudaError_t e;
   if (c->dtype == LL_FP32 || c->use_simt) {
     e = ll::launch_attend_simt(a, c->eb, st);
@@ -338,7 +339,7 @@ ll_status ll_attend_chunk(ll_cache* c, int layer, const void* q, const void* k, 
     a.mode = 2;
     a.block_tokens = c->T;
   }
-  if (ll_status s = launch_attend(c, a, st)) return s;
+  if (ll_status s = launch_attend(c, a, st, LL_KERNEL_ATTEND)) return s;
   if (!commit) return LL_OK;
 
   // Commit: frames t0 .. t0+C-1.  A frame that the same commit would already
@@ -396,7 +397,7 @@ static ll_status recache_common(ll_cache* c, int layer, const void* q_win, const
       a.La = 0;
       a.mode = 1;
     }
-    if (ll_status s = launch_attend(c, a, st)) return s;
+    if (ll_status s = launch_attend(c, a, st, LL_KERNEL_PREFILL)) return s;
   }
   std::vector<int> slot_of(R);
   for (int i = 0; i < R; ++i) slot_of[i] = ll_frame_slot(c->S, c->W, frames[i]);
