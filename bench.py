@@ -417,11 +417,14 @@ def run_ours(args, world, rank, local):
 
     def step():
         ll.ll_reset(cache)
+        st = torch.cuda.current_stream()  # the capture stream while a CUDA graph is recorded
         for c in range(chunks):
             for l in range(shape.layers):
                 q, k, v = inputs[l][c]
-                ll.ll_attend_chunk(cache, l, q, k, v, outs[l], True, stream)
+                ll.ll_attend_chunk(cache, l, q, k, v, outs[l], True, st)
 
+    if args.graph:
+        return run_graph(args, world, local, ll, cache, step, step_frames, step_flops, shape, L, chunks)
     ms, clocks, launches, prof = timed_region(args, world, local, [cache], step)
     ms_max = max_over_ranks(ms, world)
     n_att, ms_att = prof[ll.LL_KERNEL_ATTEND]
@@ -457,6 +460,38 @@ def run_ours(args, world, rank, local):
         rate, threads, sample = oracle_rate(shape)
         result["cpu_baseline"] = {"value": step_frames / (step_flops / rate), "unit": UNIT, "cores": threads,
                                   "kind": "oracle", "sample": sample}
+    return result
+
+
+def run_graph(args, world, local, ll, cache, step, step_frames, step_flops, shape, L, chunks):
+    """The whole stream step (600 attention calls from an empty cache) recorded once as one
+    CUDA graph after an eager warm-up step; every timed step replays it.  The library keeps its
+    frame bookkeeping on the host, so the graph replays exactly the calls it recorded."""
+    step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    n0 = ll.ll_launch_count()
+    with torch.cuda.graph(g):
+        step()
+    per_step = ll.ll_launch_count() - n0
+    ms, clocks, _, _ = timed_region(args, world, local, [cache], g.replay)
+    ms_max = max_over_ranks(ms, world)
+    H, d = shape.heads, shape.head_dim
+    config = {"workload": "stream30 as one CUDA graph: 30 layers x 20 chunks (60 latent frames), H=12, d=128, "
+                          "T=1560, C=3, S=3, W=9, 1 committed pass per chunk"}
+    config.update(shape_config(shape, {"chunks": chunks, "chunk_mask": args.chunk_mask,
+                                       "l2": "inputs larger than L2 (%.1f GB q/k/v)" % (
+                                           3 * L * H * d * 2 * chunks * shape.layers / 1e9),
+                                       "parallelism": "replicas x%d (independent streams, no collective)" % world}))
+    result = base_result(args, world, step_frames * args.steps * world / (ms_max / 1e3), ms_max, config)
+    result.update({
+        "tflops": step_flops * args.steps * world / (ms_max / 1e3) / 1e12,
+        "roofline": None,
+        "roofline_note": "per-kernel event brackets are not recorded in graph mode; see the eager run",
+        "gpu_launches": per_step * args.steps,
+        "clocks": clocks,
+    })
+    cache.close()
     return result
 
 
@@ -742,6 +777,8 @@ def main():
     ap.add_argument("--workload", choices=["stream30", "single", "recache30", "sweep"], default="stream30",
                     help="stream30 (default: the 30-layer stack the metric names); the others time the "
                          "single-layer, prompt-switch recache and window/sink sweep workloads")
+    ap.add_argument("--graph", action="store_true",
+                    help="stream30: record the whole step as one CUDA graph and time its replays")
     ap.add_argument("--chunk-mask", choices=["chunk", "frame"], default="chunk",
                     help="chunk (default): a chunk sees all its frames; frame: the frame-causal reading")
     ap.add_argument("--recache-scope", choices=["resident", "window"], default="resident",

@@ -1,0 +1,65 @@
+"""A stream of ll_attend_chunk calls recorded as one CUDA graph replays the same work.
+
+The library keeps its frame bookkeeping on the host and enqueues plain kernel
+launches, so a whole stream step from an empty cache (every layer, every chunk,
+each pass committing) can be recorded with torch.cuda.graph and replayed; the
+replay's outputs and raw cache bytes must equal an eager run's bit for bit.
+"""
+
+import pytest
+import torch
+
+import llsynth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ll():
+    from windowed_sink_attention_ll_b300 import build_lib
+
+    build_lib.build()
+    import windowed_sink_attention_ll_b300 as mod
+
+    mod._lib()
+    torch.cuda.set_device(0)
+    return mod
+
+
+@pytest.mark.parametrize("mask", ["chunk", "frame"])
+def test_stream_replayed_from_a_cuda_graph_equals_eager(ll, mask):
+    layers, H, D, T, S, W, C, chunks = 2, 12, 128, 1040, 3, 6, 3, 6  # 156 items: split tail too
+    L = C * T
+    cache = ll.ll_cache_create(layers, H, D, T, S, W, C, ll.LL_BF16)
+    ll.ll_set_chunk_mask(cache, mask)
+    inputs = [[tuple(llsynth.seeded_normal(("graph", l, c, t), (L, H, D), device="cuda") for t in "qkv")
+               for c in range(chunks)] for l in range(layers)]
+    outs = [[torch.empty((L, H, D), dtype=torch.bfloat16, device="cuda") for _ in range(chunks)]
+            for _ in range(layers)]
+
+    def step():
+        ll.ll_reset(cache)
+        st = torch.cuda.current_stream()
+        for c in range(chunks):
+            for l in range(layers):
+                ll.ll_attend_chunk(cache, l, *inputs[l][c], outs[l][c], True, st)
+
+    step()
+    torch.cuda.synchronize()
+    eager = [[o.clone() for o in row] for row in outs]
+    eager_raw = [ll.ll_cache_read(cache, l) for l in range(layers)]
+    for row in outs:
+        for o in row:
+            o.fill_(float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        step()
+    for _ in range(2):  # replay twice: the second replay starts from the first one's cache
+        g.replay()
+        torch.cuda.synchronize()
+        for l in range(layers):
+            for c in range(chunks):
+                assert torch.equal(outs[l][c], eager[l][c]), (l, c)
+            k, v = ll.ll_cache_read(cache, l)
+            assert torch.equal(k, eager_raw[l][0]) and torch.equal(v, eager_raw[l][1]), l
+    cache.close()
