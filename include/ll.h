@@ -230,16 +230,20 @@ LL_API ll_status ll_debug_use_simt(ll_cache* cache, int enable);
 
 /*
  * Test hook (host only, no device needed): replay the work schedule of a
- * tensor-core attend launch with Lq queries, La cached and Lb chunk keys per
- * head and at most max_ctas CTAs.  Writes the CTA count to *grid, the pieces
- * of work as (cta, item, first key tile, end key tile, partial, scratch slot)
- * sextuples into pieces[cap], and the items split across CTAs as (item, parts,
- * slot of each part ...) into splits[split_cap] (*split_ints = ints written).
- * Returns the number of pieces (-1 on bad arguments).  Items are
- * (head, 256-row query block), head-major; key tiles hold 128 keys.
+ * tensor-core attention launch with Lq queries, La cached and Lb fresh keys
+ * per head and at most max_ctas CTAs; mode 0 = chunk attend (persistent:
+ * whole rounds, then the left-over items split into runs of key tiles),
+ * mode 1 = recache prefill (La = 0, block-causal in blocks of block_tokens;
+ * persistent, items longest first in zigzag rounds, none split).  Writes the
+ * CTA count to *grid, the pieces of work as (cta, item, first key tile, end key
+ * tile, partial, scratch slot) sextuples into pieces[cap], and the items split
+ * across CTAs as (item, parts, slot of each part ...) into splits[split_cap]
+ * (*split_ints = ints written).  Returns the number of pieces (-1 on bad
+ * arguments).  Items are (head, 256-row query block): head-major in mode 0,
+ * last query block first in mode 1; key tiles hold 128 keys.
  */
-LL_API int ll_debug_attend_schedule(int Lq, int La, int Lb, int heads, int max_ctas, int* grid, int* pieces,
-                                    int cap, int* splits, int split_cap, int* split_ints);
+LL_API int ll_debug_attend_schedule(int Lq, int La, int Lb, int heads, int max_ctas, int mode, int block_tokens,
+                                    int* grid, int* pieces, int cap, int* splits, int split_cap, int* split_ints);
 
 /*
  * ll_attend_chunk_noalloc -- the attention of ll_attend_chunk (no commit) for

@@ -74,3 +74,38 @@ def test_schedule_splits_only_leftover_items(ll):
     whole = {p[1] for p in pieces if not p[4]}
     assert set(range(148)) <= whole
     assert all(item >= 148 for item, _ in splits)
+
+
+PREFILL = [
+    # Lq,    block, heads, max_ctas
+    (18720, 4680, 12, 148),   # Wan-shaped switch: 12 frames in blocks of 3 frames, 888 items
+    (18720, 1560, 12, 148),   # frame-causal blocks
+    (14040, 4680, 12, 148),   # 9 frames
+    (144, 48, 2, 148),        # tiny: fewer items than SMs
+    (300, 100, 2, 3),         # few CTAs
+]
+
+
+@pytest.mark.parametrize("shape", PREFILL, ids=[str(s) for s in PREFILL])
+def test_prefill_schedule_covers_every_item_once_and_balances(ll, shape):
+    Lq, block, H, max_ctas = shape
+    grid, pieces, splits = ll.ll_debug_attend_schedule(Lq, 0, Lq, H, max_ctas, mode=1, block_tokens=block)
+    nqb = -(-Lq // 256)
+    items = nqb * H
+    assert grid == min(max_ctas, items) and splits == []
+    seen = collections.Counter()
+    load = collections.Counter()
+    for cta, item, j0, j1, partial, slot in pieces:
+        assert 0 <= cta < grid and 0 <= item < items and j0 == 0 and partial == 0
+        qb = nqb - 1 - item // H                       # last query block first
+        last_row = min(Lq, (qb + 1) * 256) - 1
+        kv_end = min(Lq, (last_row // block + 1) * block)
+        assert j1 == -(-kv_end // 128)                 # exactly the key tiles the block may see
+        seen[item] += 1
+        load[cta] += j1
+    assert len(seen) == items and set(seen.values()) == {1}
+    # zigzag rounds over items sorted longest first: no CTA carries much more than the mean
+    if items > grid:
+        mean = sum(load.values()) / grid
+        longest = max(j for _, _, _, j, _, _ in pieces)
+        assert max(load.values()) <= mean + longest

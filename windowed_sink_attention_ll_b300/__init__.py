@@ -81,7 +81,7 @@ def _lib() -> ctypes.CDLL:
             "ll_debug_use_simt": (i32, [vp, i32]),
             "ll_profile_enable": (i32, [vp, i32]),
             "ll_set_output_dtype": (i32, [vp, i32]),
-            "ll_debug_attend_schedule": (i32, [i32, i32, i32, i32, i32, ctypes.POINTER(i32),
+            "ll_debug_attend_schedule": (i32, [i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32),
                                                ctypes.POINTER(i32), i32, ctypes.POINTER(i32), i32,
                                                ctypes.POINTER(i32)]),
             "ll_profile_read": (i32, [vp, i32, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]),
@@ -307,8 +307,9 @@ def ll_set_recache_scope(cache: LLCache, scope) -> None:
     cache.recache_scope = scope
 
 
-def ll_debug_attend_schedule(Lq: int, La: int, Lb: int, heads: int, max_ctas: int):
-    """Host replay of a tensor-core attend launch's schedule (see include/ll.h).
+def ll_debug_attend_schedule(Lq: int, La: int, Lb: int, heads: int, max_ctas: int, mode: int = 0,
+                             block_tokens: int = 1):
+    """Host replay of a tensor-core attend (mode 0) or prefill (mode 1) launch's schedule (see include/ll.h).
 
     Returns (grid, pieces, splits): pieces = list of (cta, item, j0, j1, partial,
     slot); splits = list of (item, [slots of its parts]).
@@ -317,8 +318,8 @@ def ll_debug_attend_schedule(Lq: int, La: int, Lb: int, heads: int, max_ctas: in
     pieces = (ctypes.c_int * cap)()
     splits = (ctypes.c_int * scap)()
     grid, nints = ctypes.c_int(), ctypes.c_int()
-    n = _lib().ll_debug_attend_schedule(Lq, La, Lb, heads, max_ctas, ctypes.byref(grid), pieces, cap, splits,
-                                        scap, ctypes.byref(nints))
+    n = _lib().ll_debug_attend_schedule(Lq, La, Lb, heads, max_ctas, mode, block_tokens, ctypes.byref(grid), pieces,
+                                        cap, splits, scap, ctypes.byref(nints))
     if n < 0:
         raise LLError(LL_ERR_INVALID_ARG, "ll_debug_attend_schedule")
     out = [tuple(pieces[6 * i:6 * i + 6]) for i in range(n)]

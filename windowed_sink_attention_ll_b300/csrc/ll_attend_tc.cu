@@ -328,16 +328,14 @@ struct Piece {
 struct Walker {
   int r;
   long long it, end, begin;
-  int single;
-  int done;
+  int prefill;
 };
 
 __host__ __device__ __forceinline__ void walker_init(Walker& w, const TcParams& p, int cta) {
   w.r = 0;
-  w.done = 0;
-  w.single = p.a.mode == 1;
+  w.prefill = p.a.mode == 1;
   w.begin = w.end = 0;
-  if (!w.single && cta < p.tail_ctas) {
+  if (!w.prefill && cta < p.tail_ctas) {
     w.begin = (p.tail_iters * cta) / p.tail_ctas;
     w.end = (p.tail_iters * (cta + 1)) / p.tail_ctas;
   }
@@ -354,15 +352,22 @@ __host__ __device__ __forceinline__ int prefill_nkv(const TcParams& p, int qb) {
 }
 
 __host__ __device__ __forceinline__ bool walker_next(Walker& w, const TcParams& p, Piece& pc, int cta) {
-  if (w.single) {
-    if (w.done) return false;
-    w.done = 1;
-    pc.item = cta;
-    pc.j0 = 0;
-    pc.j1 = prefill_nkv(p, p.nqb - 1 - cta / p.a.heads);
-    pc.partial = 0;
-    pc.slot = 0;
-    return true;
+  if (w.prefill) {
+    // items come longest first; round r hands them out left to right (even r) or
+    // right to left (odd r), so each CTA's total stays close to the mean
+    const int items = p.nqb * p.a.heads;
+    while (w.r * p.grid < items) {
+      const int r = w.r++;
+      const int item = r * p.grid + ((r & 1) ? p.grid - 1 - cta : cta);
+      if (item >= items) continue;
+      pc.item = item;
+      pc.j0 = 0;
+      pc.j1 = prefill_nkv(p, p.nqb - 1 - item / p.a.heads);
+      pc.partial = 0;
+      pc.slot = 0;
+      return true;
+    }
+    return false;
   }
   if (w.r < p.rounds) {
     pc.item = w.r * p.grid + cta;
@@ -918,7 +923,10 @@ cudaError_t launch_tc(const AttendArgs& a, cudaStream_t stream) {
   CombineParams cp;
   cp.nsplit = 0;
   if (a.mode == 1) {
-    p.grid = p.nqb * a.heads;
+    // persistent: one CTA per SM, items in zigzag rounds (see walker_next)
+    const int items = p.nqb * a.heads;
+    const int sms = sm_count();
+    p.grid = items < sms ? items : sms;
   } else {
     // without scratch for two partial results per CTA, no item is split
     int ctas = sm_count();
@@ -964,17 +972,25 @@ int attend_scratch_slots_wanted() {
   return 2 * n;
 }
 
-int attend_schedule_dump(int Lq, int La, int Lb, int heads, int max_ctas, int* grid, int* out, int cap,
-                         int* splits, int split_cap, int* split_ints) {
+int attend_schedule_dump(int Lq, int La, int Lb, int heads, int max_ctas, int mode, int block_tokens, int* grid,
+                         int* out, int cap, int* splits, int split_cap, int* split_ints) {
   TcParams p;
   std::memset(&p, 0, sizeof(p));
   p.a.Lq = Lq;
   p.a.La = La;
   p.a.Lb = Lb;
   p.a.heads = heads;
+  p.a.mode = mode;
+  p.a.block_tokens = block_tokens;
   p.nqb = (Lq + NQ * BM - 1) / (NQ * BM);
   CombineParams cp;
-  plan_attend(p, cp, max_ctas);
+  cp.nsplit = 0;
+  if (mode == 1) {
+    const int items = p.nqb * heads;
+    p.grid = items < max_ctas ? items : max_ctas;
+  } else {
+    plan_attend(p, cp, max_ctas);
+  }
   *grid = p.grid;
   int n = 0;
   for (int c = 0; c < p.grid; ++c) {

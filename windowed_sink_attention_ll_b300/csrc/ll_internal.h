@@ -74,10 +74,11 @@ cudaError_t launch_attend_bf16_tc(const AttendArgs& a, cudaStream_t stream);
 // slot count it uses on the current device (two per SM).
 size_t attend_scratch_bytes(int head_dim, int slots);
 int attend_scratch_slots_wanted();
-// Host replay of the attend schedule (tests): pieces as (cta, item, j0, j1,
-// partial, slot) sextuples, split items as (item, parts, slots...).
-int attend_schedule_dump(int Lq, int La, int Lb, int heads, int max_ctas, int* grid, int* out, int cap,
-                         int* splits, int split_cap, int* split_ints);
+// Host replay of the schedule of an attend (mode 0) or prefill (mode 1) launch
+// (tests): pieces as (cta, item, j0, j1, partial, slot) sextuples, split items
+// as (item, parts, slots...).
+int attend_schedule_dump(int Lq, int La, int Lb, int heads, int max_ctas, int mode, int block_tokens, int* grid,
+                         int* out, int cap, int* splits, int split_cap, int* split_ints);
 cudaError_t launch_attend_simt(const AttendArgs& a, int elem_bytes, cudaStream_t stream);
 
 void count_launch();
