@@ -15,12 +15,14 @@
 // attend schedule and every cached key, and masks the chunk's own keys the
 // same block-causal way (the frame-causal chunk and the keep-sink prefill).
 //
-// CTA = one head x 256 query rows (two 128-row tiles that share every K/V
-// tile).  Attend launches are persistent: whole rounds of items, then the
-// left-over items split into runs of key tiles merged by combine_kernel (see
-// "Work schedule").  Warp roles (384 threads):
+// Work item = one head x 256 query rows (two 128-row tiles that share every
+// K/V tile); one CTA per SM walks several items (see "Work schedule"):
+// attend launches run whole rounds of items, then split the left-over items
+// into runs of key tiles merged by combine_kernel; prefill launches hand out
+// their unequal items longest first in zigzag rounds.  Warp roles (384 threads):
 //   warp 0      TMA producer: Q per item, then K0 V0 K1 V1 ... into a 5-stage ring
-//   warp 1      TMEM allocator and tcgen05.mma issuer (one thread)
+//   warp 1      TMEM allocator; one thread issues tcgen05.mma, eight k-steps
+//               per asm block with every descriptor ready in registers
 //   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: thread = row
 //   warps 2-3   idle
 // Tensor memory (512 columns x 128 lanes): O0 [0,128) O1 [128,256)
@@ -316,8 +318,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
 // into equal runs of key tiles across `tail_ctas` CTAs.  A run that covers only
 // part of an item leaves a partial result (unnormalised O, reference max m and
 // sum l per row) in scratch slot 2*c + (0: first run of CTA c, 1: its last
-// run); combine_kernel merges the parts of each split item.
-// Prefill mode: one item per CTA, the longest query blocks first.
+// run); combine_kernel merges the parts of each split item.  Mode 2 (masked
+// attend) uses the same schedule.
+// Prefill mode (mode 1): items are numbered from the last query block to the
+// first, i.e. longest first (block g of a block-causal prefill sees g + 1
+// blocks of keys); round r gives CTA c item r*grid + c (r even) or
+// r*grid + grid - 1 - c (r odd), which keeps every CTA's total within one item
+// of the mean without splitting any item.
 struct Piece {
   int item;
   int j0, j1;   // key tiles [j0, j1) of the item
