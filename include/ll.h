@@ -233,8 +233,9 @@ LL_API ll_status ll_debug_use_simt(ll_cache* cache, int enable);
  * tensor-core attention launch with Lq queries, La cached and Lb fresh keys
  * per head and at most max_ctas CTAs; mode 0 = chunk attend (persistent:
  * whole rounds, then the left-over items split into runs of key tiles),
- * mode 1 = recache prefill (La = 0, block-causal in blocks of block_tokens;
- * persistent, items longest first in zigzag rounds, none split).  Writes the
+ * mode 1 = recache prefill (La cached keys all visible, the Lb fresh keys
+ * block-causal in blocks of block_tokens; persistent, items longest first in
+ * zigzag rounds, none split).  Writes the
  * CTA count to *grid, the pieces of work as (cta, item, first key tile, end key
  * tile, partial, scratch slot) sextuples into pieces[cap], and the items split
  * across CTAs as (item, parts, slot of each part ...) into splits[split_cap]

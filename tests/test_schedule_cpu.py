@@ -77,19 +77,19 @@ def test_schedule_splits_only_leftover_items(ll):
 
 
 PREFILL = [
-    # Lq,    block, heads, max_ctas
-    (18720, 4680, 12, 148),   # Wan-shaped switch: 12 frames in blocks of 3 frames, 888 items
-    (18720, 1560, 12, 148),   # frame-causal blocks
-    (14040, 4680, 12, 148),   # 9 frames
-    (144, 48, 2, 148),        # tiny: fewer items than SMs
-    (300, 100, 2, 3),         # few CTAs
+    # Lq,    La,   block, heads, max_ctas
+    (18720, 0, 4680, 12, 148),      # Wan-shaped switch: 12 frames in blocks of 3 frames, 888 items
+    (18720, 0, 1560, 12, 148),      # frame-causal blocks
+    (14040, 4680, 4680, 12, 148),   # keep-sink switch: 9 window frames after 3 cached sink frames
+    (144, 0, 48, 2, 148),           # tiny: fewer items than SMs
+    (300, 100, 100, 2, 3),          # few CTAs, a cached prefix with a ragged last tile
 ]
 
 
 @pytest.mark.parametrize("shape", PREFILL, ids=[str(s) for s in PREFILL])
 def test_prefill_schedule_covers_every_item_once_and_balances(ll, shape):
-    Lq, block, H, max_ctas = shape
-    grid, pieces, splits = ll.ll_debug_attend_schedule(Lq, 0, Lq, H, max_ctas, mode=1, block_tokens=block)
+    Lq, La, block, H, max_ctas = shape
+    grid, pieces, splits = ll.ll_debug_attend_schedule(Lq, La, Lq, H, max_ctas, mode=1, block_tokens=block)
     nqb = -(-Lq // 256)
     items = nqb * H
     assert grid == min(max_ctas, items) and splits == []
@@ -100,7 +100,7 @@ def test_prefill_schedule_covers_every_item_once_and_balances(ll, shape):
         qb = nqb - 1 - item // H                       # last query block first
         last_row = min(Lq, (qb + 1) * 256) - 1
         kv_end = min(Lq, (last_row // block + 1) * block)
-        assert j1 == -(-kv_end // 128)                 # exactly the key tiles the block may see
+        assert j1 == -(-La // 128) + -(-kv_end // 128)  # every cached tile + the fresh tiles it may see
         seen[item] += 1
         load[cta] += j1
     assert len(seen) == items and set(seen.values()) == {1}

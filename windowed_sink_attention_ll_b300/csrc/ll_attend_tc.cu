@@ -10,10 +10,11 @@
 // the chunk's own keys].  Softmax does not depend on the order of the keys,
 // so the kernel walks the resident cache rows in slot order (one contiguous
 // run per head, see ll_host.cu) and then the chunk's rows.  In prefill mode
-// (§3.1 "KV recache") there is one source, the recache window, and query row
-// i sees key j iff j / block_tokens <= i / block_tokens.  Mode 2 keeps the
-// attend schedule and every cached key, and masks the chunk's own keys the
-// same block-causal way (the frame-causal chunk and the keep-sink prefill).
+// (§3.1 "KV recache") query row i sees every cached key (the sink rows of a
+// keep-sink prefill; none otherwise) and fresh key j iff
+// j / block_tokens <= i / block_tokens.  Mode 2 keeps the attend schedule and
+// every cached key, and masks the chunk's own keys the same block-causal way
+// (the frame-causal chunk).
 //
 // Work item = one head x 256 query rows (two 128-row tiles that share every
 // K/V tile); one CTA per SM walks several items (see "Work schedule"):
@@ -349,13 +350,15 @@ __host__ __device__ __forceinline__ void walker_init(Walker& w, const TcParams& 
   w.it = w.begin;
 }
 
+// Key tiles a prefill item of query block qb needs: every cached tile (source A,
+// fully visible) and the fresh tiles up to the end of the block of its last row.
 __host__ __device__ __forceinline__ int prefill_nkv(const TcParams& p, int qb) {
   const AttendArgs& a = p.a;
   const int qend = (qb + 1) * NQ * BM;
   const int qlast = (qend < a.Lq ? qend : a.Lq) - 1;
   const long long e = ((long long)qlast / a.block_tokens + 1) * a.block_tokens;
   const int kv_end = (int)(e < a.Lb ? e : a.Lb);
-  return (kv_end + BN - 1) / BN;
+  return (a.La + BN - 1) / BN + (kv_end + BN - 1) / BN;
 }
 
 __host__ __device__ __forceinline__ bool walker_next(Walker& w, const TcParams& p, Piece& pc, int cta) {
@@ -409,7 +412,7 @@ __device__ __forceinline__ void item_geom(const TcParams& p, int item, int& head
     const int qb = p.nqb - 1 - item / p.a.heads;
     head = item - (item / p.a.heads) * p.a.heads;
     q0 = qb * NQ * BM;
-    nA = 0;
+    nA = (p.a.La + BN - 1) / BN;
   }
 }
 

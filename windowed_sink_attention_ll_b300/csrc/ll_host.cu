@@ -389,14 +389,9 @@ static ll_status recache_common(ll_cache* c, int layer, const void* q_win, const
     a.Lb = R * c->T;
     a.Lq = R * c->T;
     a.block_tokens = (c->chunk_mask == LL_MASK_FRAME ? 1 : c->C) * c->T;
-    if (c->recache_scope == LL_RECACHE_WINDOW) {
-      // window queries see the cached sink rows (slots [0, sink)) and the fresh window
-      a.La = sink * c->T;
-      a.mode = 2;
-    } else {
-      a.La = 0;
-      a.mode = 1;
-    }
+    // keep-sink scope: the window queries also see the cached sink rows (slots [0, sink))
+    a.La = c->recache_scope == LL_RECACHE_WINDOW ? sink * c->T : 0;
+    a.mode = 1;
     if (ll_status s = launch_attend(c, a, st, LL_KERNEL_PREFILL)) return s;
   }
   std::vector<int> slot_of(R);
@@ -526,7 +521,7 @@ int ll_debug_attend_schedule(int Lq, int La, int Lb, int heads, int max_ctas, in
                              int* grid, int* pieces, int cap, int* splits, int split_cap, int* split_ints) {
   if (Lq < 1 || La < 0 || Lb < 1 || heads < 1 || max_ctas < 1 || !grid || !split_ints) return -1;
   if (mode != 0 && mode != 1) return -1;
-  if (mode == 1 && (La != 0 || block_tokens < 1)) return -1;
+  if (mode == 1 && block_tokens < 1) return -1;
   return ll::attend_schedule_dump(Lq, La, Lb, heads, max_ctas, mode, block_tokens, grid, pieces, cap, splits,
                                   split_cap, split_ints);
 }

@@ -40,10 +40,10 @@ cudaError_t launch_copy_frames(const CopyFramesArgs& a, cudaStream_t stream);
 //   source B: rows [0, Lb) of a caller tensor [Lb][H][d] (the chunk's own K/V,
 //             or the recache window in prefill mode).
 // mode 0 (attend): every query sees all La + Lb keys.
-// mode 1 (prefill): La = 0 and query row i sees keys j of source B with
-//             j / block_tokens <= i / block_tokens.
-// mode 2 (masked attend): every key of source A, and keys j of source B with
-//             j / block_tokens <= i / block_tokens (attend schedule).
+// mode 1 (prefill): every key of source A (La = 0 except in the keep-sink
+//             prefill) and keys j of source B with j / block_tokens <=
+//             i / block_tokens (prefill schedule: unequal items, none split).
+// mode 2 (masked attend): the same mask with the attend schedule.
 // ---------------------------------------------------------------------------
 struct AttendArgs {
   const void* q;      // [Lq][H][d]
