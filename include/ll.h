@@ -263,7 +263,8 @@ LL_API int ll_debug_attend_schedule(int Lq, int La, int Lb, int heads, int max_c
  * cudaFree, no allocating library routine.
  *
  * Per head h: out_h = softmax(q_h K_h^T / sqrt(d)) V_h over the keys
- * [cached rows || the chunk's own rows], bf16 in and out, fp32 softmax.
+ * [cached rows || the chunk's own rows], every query seeing every key (the
+ * default chunk mask), bf16 in and out, fp32 softmax.
  *   q, k, v, out: [chunk_tokens][heads][head_dim] bf16 device buffers (16-byte
  *                 aligned; out may not alias q, k or v).
  *   k_cached, v_cached: the resident rows, head-major: head h's cached_tokens

@@ -170,3 +170,15 @@ def test_window_scope_without_window_frames_is_a_state_error(ll):
         ll.ll_recache(st.cache, 0, k, v)
     assert e.value.status == ll.LL_ERR_STATE
     st.close()
+
+
+def test_option_setters_reject_unknown_values(ll):
+    cache = ll.ll_cache_create(1, 2, 64, 16, 3, 6, 3, ll.LL_BF16)
+    for setter in (ll.ll_set_chunk_mask, ll.ll_set_recache_scope):
+        for bad in (-1, 2, 7):
+            with pytest.raises(ll.LLError) as e:
+                setter(cache, bad)
+            assert e.value.status == ll.LL_ERR_INVALID_ARG
+    ll.ll_set_chunk_mask(cache, "frame")
+    ll.ll_set_recache_scope(cache, "window")
+    cache.close()
