@@ -30,3 +30,25 @@ def read_golden(name):
 @pytest.fixture
 def golden():
     return read_golden
+
+
+@pytest.fixture(autouse=True)
+def _tag_parity_records(request):
+    """Label the parity records a test makes with the test's id (see tests/gpu_util.py)."""
+    yield
+    mod = sys.modules.get("tests.gpu_util")
+    if mod is not None:
+        for rec in mod.OBSERVED:
+            rec.setdefault("test", request.node.nodeid)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With LL_PARITY_LOG set, write every GPU parity comparison (test, check, errors) as JSON."""
+    path = os.environ.get("LL_PARITY_LOG")
+    mod = sys.modules.get("tests.gpu_util")
+    if not path or mod is None:
+        return
+    import json
+
+    with open(path, "w") as f:
+        json.dump(mod.OBSERVED, f)

@@ -21,6 +21,11 @@ def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
     return np.exp2(np.floor(np.log2(ax)) - 8)
 
 
+# Every comparison's max |err| and relative L2, per test (written out by tests/conftest.py when
+# LL_PARITY_LOG names a file).
+OBSERVED = []
+
+
 def compare(got: torch.Tensor, want: np.ndarray, what: str, atol=ATOL, rel_l2=REL_L2):
     """max|err| <= atol and relative L2 <= rel_l2.  atol=None (bf16 outputs of large
     magnitude): each element may also carry the half-ulp of rounding it to bf16."""
@@ -30,6 +35,8 @@ def compare(got: torch.Tensor, want: np.ndarray, what: str, atol=ATOL, rel_l2=RE
     diff = np.abs(g - want)
     err = float(diff.max())
     rel = float(np.linalg.norm(g - want) / max(np.linalg.norm(want), 1e-30))
+    OBSERVED.append({"what": what, "max_abs_err": err, "rel_l2": rel, "max_abs_out": float(np.abs(want).max()),
+                     "bf16_out": atol is None})
     if atol is None:
         excess = float((diff - bf16_half_ulp(want)).max())
         assert excess <= ATOL and rel <= rel_l2, (
