@@ -198,10 +198,13 @@ LL_API int ll_resident_frames(int sink_frames, int window_frames, int64_t n, int
 LL_API uint64_t ll_launch_count(void);
 
 /*
- * Per-kernel timing.  While profiling is on, each kernel this cache launches is
- * bracketed by two CUDA events on its stream.  ll_profile_read synchronises,
- * returns for one kernel kind the number of launches and their summed device
- * time (milliseconds) since profiling was switched on, and clears that kind.
+ * Per-kernel timing.  ll_profile_enable(cache, n) with n > 0 brackets one
+ * launch in every n of each kind (the first, the (n+1)-th, ...) with two CUDA
+ * events on its stream; n = 1 brackets every launch, n <= 0 switches timing
+ * off.  ll_profile_read synchronises, returns for one kernel kind the number of
+ * bracketed launches and their summed device time (milliseconds) since timing
+ * was switched on, and clears that kind.  An attend bracket also holds the
+ * merge of split work items that follows the attention kernel.
  */
 typedef enum {
   LL_KERNEL_ATTEND = 0,  /* chunk attention (tensor-core or fp32 kernel) */

@@ -273,8 +273,9 @@ def ll_debug_use_simt(cache: LLCache, enable: bool) -> None:
     _check(_lib().ll_debug_use_simt(cache.ptr, 1 if enable else 0), "ll_debug_use_simt")
 
 
-def ll_profile_enable(cache: LLCache, enable: bool) -> None:
-    _check(_lib().ll_profile_enable(cache.ptr, 1 if enable else 0), "ll_profile_enable")
+def ll_profile_enable(cache: LLCache, enable, every: int = 1) -> None:
+    """Time one launch in every `every` of each kind (enable=False: off)."""
+    _check(_lib().ll_profile_enable(cache.ptr, max(1, int(every)) if enable else 0), "ll_profile_enable")
 
 
 def ll_profile_read(cache: LLCache, kind: int):

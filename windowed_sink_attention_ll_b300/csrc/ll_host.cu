@@ -53,6 +53,8 @@ struct ll_cache {
     cudaEvent_t start, stop;
   };
   bool profiling = false;
+  int profile_every = 1;                    // bracket one launch in every `profile_every` of a kind
+  uint64_t profile_seen[LL_KERNEL_KINDS] = {0, 0, 0};
   std::vector<Mark> marks;
   std::vector<cudaEvent_t> event_pool;
 };
@@ -126,7 +128,9 @@ struct ProfileScope {
   int kind;
   cudaEvent_t start = nullptr;
   ProfileScope(ll_cache* c_, cudaStream_t st_, int kind_) : c(c_), st(st_), kind(kind_) {
-    if (c->profiling && (start = pooled_event(c)) != nullptr) cudaEventRecord(start, st);
+    if (!c->profiling) return;
+    if (c->profile_seen[kind]++ % (uint64_t)c->profile_every != 0) return;  // not sampled
+    if ((start = pooled_event(c)) != nullptr) cudaEventRecord(start, st);
   }
   void done() {
     if (!start) return;
@@ -488,7 +492,11 @@ ll_status ll_debug_inject_stall(ll_cache* c, int enable, int timeout_us) {
 
 ll_status ll_profile_enable(ll_cache* c, int enable) {
   if (!c) return LL_ERR_INVALID_ARG;
-  c->profiling = enable != 0;
+  c->profiling = enable > 0;
+  if (enable > 0) {
+    c->profile_every = enable;
+    for (auto& n : c->profile_seen) n = 0;
+  }
   return LL_OK;
 }
 
