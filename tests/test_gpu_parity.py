@@ -268,3 +268,21 @@ def test_sweep_long_horizon(ll, W, S):
             st.check_state()
     st.check_state()
     st.close()
+
+
+def test_long_window_many_keys(ll):
+    """A 64-frame window: each chunk attends to 70 frames = 109200 keys (about 850 key tiles per
+    work item, 4.7x the longest sweep list); 8 heads x 19 query blocks = 152 items on the SMs,
+    so the left-over items are split and merged with very long runs."""
+    H, D, T, S, W, C = 8, 128, 1560, 3, 64, 3
+    st = Lockstep(ll, 1, H, D, T, S, W, C, torch.bfloat16)
+    shape = llsynth.Shape(1, H, D, T, S, W, C)
+    n_fill = (S + W) // C + 1
+    for c in range(n_fill):  # fill the sink and the window (first evictions included)
+        st.attend(0, *wan_chunk("long", 0, c, shape), commit=True, check=False)
+    assert st.orc.state(0)[0] == n_fill * C
+    rows = sample_rows(C * T, 128, seed=5)
+    st.attend(0, *wan_chunk("long-q", 0, n_fill, shape), commit=True, rows=rows, what="long window attend")
+    st.check_state()
+    st.check_raw(0)
+    st.close()
