@@ -92,7 +92,8 @@ LL_API void ll_cache_destroy(ll_cache* cache);
  *   out_h = softmax(q_h K_h^T / sqrt(d)) V_h,
  *   K/V = [frames 0..min(S,t0)-1 || frames max(S,t0-W)..t0-1 || k/v of this chunk].
  * q, k, v: [C*T][H][d] device buffers in the cache dtype; out: [C*T][H][d] in
- * the output dtype (see ll_set_output_dtype); out may not alias q, k or v.
+ * the output dtype (see ll_set_output_dtype); out may share no byte with q,
+ * k or v (LL_ERR_INVALID_ARG).
  * commit != 0: after the attention, the chunk's K/V are written into the
  * cache: frame f < S into sink slot f, frame f >= S into ring slot
  * S + ((f - S) mod W), replacing the frame W positions older; frames that
@@ -117,7 +118,8 @@ LL_API ll_status ll_recache(ll_cache* cache, int layer, const void* k_win, const
 /*
  * ll_recache_attend -- the recache prefill: block-causal attention over the
  * R resident frames' fresh q/k/v (list cut into blocks of C frames; query
- * rows of block g see key blocks 0..g), written to out_win [R*T][H][d];
+ * rows of block g see key blocks 0..g), written to out_win [R*T][H][d]
+ * (sharing no byte with q_win, k_win or v_win: LL_ERR_INVALID_ARG);
  * then the same K/V write as ll_recache.
  */
 LL_API ll_status ll_recache_attend(ll_cache* cache, int layer, const void* q_win, const void* k_win,
@@ -269,7 +271,8 @@ LL_API int ll_debug_attend_schedule(int Lq, int La, int Lb, int heads, int max_c
  * [cached rows || the chunk's own rows], every query seeing every key (the
  * default chunk mask), bf16 in and out, fp32 softmax.
  *   q, k, v, out: [chunk_tokens][heads][head_dim] bf16 device buffers (16-byte
- *                 aligned; out may not alias q, k or v).
+ *                 aligned; out may share no byte with q, k, v or the
+ *                 cached rows: LL_ERR_INVALID_ARG).
  *   k_cached, v_cached: the resident rows, head-major: head h's cached_tokens
  *                 rows of head_dim elements start at element
  *                 h * cached_head_stride (16-byte aligned, stride a multiple

@@ -117,3 +117,28 @@ def test_binding_rejects_host_tensors(ll):
     t = torch.zeros(48, 2, 64, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         ll.ll_attend_chunk(cache, 0, t, t, t, t, True)
+
+
+def test_noalloc_rejects_an_output_that_overlaps_an_input(ll):
+    """Byte-range checks of ll_attend_chunk_noalloc.  They run before the call looks
+    at a device: every overlapping case returns LL_ERR_INVALID_ARG, and each
+    control without the overlap stops at the head_dim check (96: LL_ERR_UNSUPPORTED).
+    The addresses are never dereferenced and nothing is enqueued."""
+    lib = ll._lib()
+    L, H, d = 64, 2, 96
+    nb = L * H * d * 2  # bytes of q, k, v and out
+    base = 1 << 40
+    q, k, v = base, base + (1 << 20), base + (2 << 20)
+    kc, vc = base + (8 << 20), base + (12 << 20)
+    cached, stride = 100, 100 * d
+    cb = ((H - 1) * stride + cached * d) * 2  # bytes spanned by the cached rows of all heads
+
+    def call(out, cached_tokens=cached):
+        return lib.ll_attend_chunk_noalloc(q, kc, vc, cached_tokens, stride, k, v, L, out, H, d, None, None)
+
+    for out in (q, q + 16, q - nb + 16, k + nb - 16, v - nb + 16, kc + cb - 16, vc - nb + 16):
+        assert call(out) == ll.LL_ERR_INVALID_ARG, hex(out - base)
+    for out in (base + (4 << 20), q + nb, q - nb, kc + cb, vc - nb):
+        assert call(out) == ll.LL_ERR_UNSUPPORTED, hex(out - base)
+    # with no cached rows the cached pointers are ignored
+    assert call(kc, cached_tokens=0) == ll.LL_ERR_UNSUPPORTED

@@ -150,6 +150,66 @@ def test_reset_and_empty_recache(ll):
     st.close()
 
 
+def test_output_sharing_bytes_with_an_input_is_rejected(ll):
+    """An output that shares any byte with an input (q, k, v; q_win, k_win, v_win) is
+    rejected before anything is enqueued, and the cache is left as it was.  All
+    tensors are views of one allocation with the inputs at byte offsets 2nb, 3nb,
+    4nb (nb = bytes of one bf16 input), so no case reaches outside it."""
+    H, D, T, S, W, C = 2, 64, 16, 3, 6, 3
+    st = Lockstep(ll, 1, H, D, T, S, W, C, torch.bfloat16)
+
+    def buffer(rows, tag):
+        nb = rows * H * D * 2
+        raw = torch.zeros(8 * nb, dtype=torch.uint8, device="cuda")
+
+        def at(off, dt=torch.bfloat16):
+            size = nb * (2 if dt == torch.float32 else 1)
+            return raw[off:off + size].view(dt).view(rows, H, D)
+
+        ins = [at(i * nb) for i in (2, 3, 4)]
+        for t, name in zip(ins, "qkv"):
+            t.copy_(llsynth.seeded_normal((tag, name), (rows, H, D), device="cuda"))
+        return nb, at, ins
+
+    L = C * T
+    nb, at, (q, k, v) = buffer(L, "overlap")
+    for off in (nb + 16, 2 * nb + 16, 3 * nb - 16, 4 * nb + 16, 5 * nb - 16):
+        with pytest.raises(ll.LLError) as e:
+            ll.ll_attend_chunk(st.cache, 0, q, k, v, at(off), True)
+        assert e.value.status == ll.LL_ERR_INVALID_ARG, off
+    # an fp32 output is 2nb long: at byte 16 it ends 16 bytes inside q
+    ll.ll_set_output_dtype(st.cache, torch.float32)
+    with pytest.raises(ll.LLError) as e:
+        ll.ll_attend_chunk(st.cache, 0, q, k, v, at(16, torch.float32), True)
+    assert e.value.status == ll.LL_ERR_INVALID_ARG
+    st.check_state()
+    # outputs that end at q's first byte or start after v's last are accepted
+    want = st.orc.attend(0, f64(q), f64(k), f64(v), False)
+    out32 = at(0, torch.float32)
+    ll.ll_attend_chunk(st.cache, 0, q, k, v, out32, False)
+    compare(out32, want, "fp32 out ending where q starts")
+    ll.ll_set_output_dtype(st.cache, torch.bfloat16)
+    out = at(5 * nb)
+    st.orc.attend(0, f64(q), f64(k), f64(v), True)  # same pass, committed on both sides
+    ll.ll_attend_chunk(st.cache, 0, q, k, v, out, True)
+    compare(out, want, "bf16 out starting after v")
+    st.host[0].update({i: (k[i * T:(i + 1) * T].cpu(), v[i * T:(i + 1) * T].cpu()) for i in range(C)})
+    q2, k2, v2 = (llsynth.seeded_normal(("overlap-2", t), (L, H, D), device="cuda") for t in "qkv")
+    st.attend(0, q2, k2, v2, commit=True)
+    st.check_state()
+    st.check_raw(0)
+
+    R = 6  # resident frames after two chunks: 3 sink + 3 window
+    nbw, atw, (qw, kw, vw) = buffer(R * T, "overlap-rc")
+    for off in (nbw + 16, 3 * nbw + 16, 5 * nbw - 16):
+        with pytest.raises(ll.LLError) as e:
+            ll.ll_recache_attend(st.cache, 0, qw, kw, vw, atw(off))
+        assert e.value.status == ll.LL_ERR_INVALID_ARG, off
+    st.check_state()
+    st.check_raw(0)
+    st.close()
+
+
 # ---------------------------------------------------------------------------
 # Wan-shaped workloads at full size (sampled query rows, all heads)
 # ---------------------------------------------------------------------------

@@ -73,6 +73,24 @@ int64_t resident_count(int S, int W, int64_t n) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// true when the byte ranges [a, a + na) and [b, b + nb) share a byte
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+// An output of `rows` token rows may share no byte with the inputs of `rows` rows
+// (an input pointer may be NULL).
+bool output_overlaps_inputs(const ll_cache* c, int64_t rows, const void* out, const void* a, const void* b,
+                            const void* d) {
+  const size_t row_elems = (size_t)c->H * c->D;
+  const size_t in_bytes = (size_t)rows * row_elems * c->eb;
+  const size_t out_bytes = (size_t)rows * row_elems * ((c->dtype == LL_FP32 || c->out_f32) ? 4 : c->eb);
+  for (const void* p : {a, b, d})
+    if (p && overlap(out, out_bytes, p, in_bytes)) return true;
+  return false;
+}
+
 ll_status take_device_error(ll_cache* c) {
   volatile unsigned* e = c->err_host;
   const unsigned v = *e;
@@ -322,7 +340,7 @@ ll_status ll_attend_chunk(ll_cache* c, int layer, const void* q, const void* k, 
   if (ll_status s = check_layer(c, layer)) return s;
   if (!q || !k || !v || !out) return LL_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return LL_ERR_INVALID_ARG;
-  if (out == q || out == k || out == v) return LL_ERR_INVALID_ARG;
+  if (output_overlaps_inputs(c, (int64_t)c->C * c->T, out, q, k, v)) return LL_ERR_INVALID_ARG;
   if (ll_status s = take_device_error(c)) return s;
   if (ll_status s = set_device(c)) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -370,7 +388,6 @@ static ll_status recache_common(ll_cache* c, int layer, const void* q_win, const
   if (!k_win || !v_win) return LL_ERR_INVALID_ARG;
   if (!aligned16(k_win) || !aligned16(v_win)) return LL_ERR_INVALID_ARG;
   if (q_win && (!out_win || !aligned16(q_win) || !aligned16(out_win))) return LL_ERR_INVALID_ARG;
-  if (q_win && (out_win == q_win || out_win == k_win || out_win == v_win)) return LL_ERR_INVALID_ARG;
   const int64_t n = c->n[layer];
   std::vector<int64_t> frames(c->S + c->W + 1);
   int R = ll_resident_frames(c->S, c->W, n, frames.data());
@@ -381,6 +398,7 @@ static ll_status recache_common(ll_cache* c, int layer, const void* q_win, const
     R -= sink;
   }
   if (R == 0) return LL_ERR_STATE;
+  if (q_win && output_overlaps_inputs(c, (int64_t)R * c->T, out_win, q_win, k_win, v_win)) return LL_ERR_INVALID_ARG;
   if (ll_status s = take_device_error(c)) return s;
   if (ll_status s = set_device(c)) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -58,6 +58,12 @@ ll_status scratch_address(int dev, unsigned char** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// true when the byte ranges [a, a + na) and [b, b + nb) share a byte
+bool overlap(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
 }  // namespace
 
 extern "C" ll_status ll_attend_chunk_noalloc(const void* q, const void* k_cached, const void* v_cached,
@@ -66,8 +72,20 @@ extern "C" ll_status ll_attend_chunk_noalloc(const void* q, const void* k_cached
                                              int head_dim, unsigned* err_word, void* stream) {
   if (!q || !k || !v || !out) return LL_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return LL_ERR_INVALID_ARG;
-  if (out == q || out == k || out == v) return LL_ERR_INVALID_ARG;
   if (heads < 1 || chunk_tokens < 1 || cached_tokens < 0) return LL_ERR_INVALID_ARG;
+  // out shares no byte with any input (bf16 rows of heads * head_dim elements)
+  if (head_dim > 0) {
+    const size_t chunk_bytes = (size_t)chunk_tokens * heads * head_dim * 2;
+    if (overlap(out, chunk_bytes, q, chunk_bytes) || overlap(out, chunk_bytes, k, chunk_bytes) ||
+        overlap(out, chunk_bytes, v, chunk_bytes))
+      return LL_ERR_INVALID_ARG;
+    if (cached_tokens > 0 && cached_head_stride > 0) {
+      const size_t cached_bytes = ((size_t)(heads - 1) * cached_head_stride + (size_t)cached_tokens * head_dim) * 2;
+      if ((k_cached && overlap(out, chunk_bytes, k_cached, cached_bytes)) ||
+          (v_cached && overlap(out, chunk_bytes, v_cached, cached_bytes)))
+        return LL_ERR_INVALID_ARG;
+    }
+  }
   if (head_dim != 64 && head_dim != 128) return LL_ERR_UNSUPPORTED;
   if ((int64_t)cached_tokens + chunk_tokens > (1LL << 30)) return LL_ERR_UNSUPPORTED;
   if (cached_tokens > 0) {
