@@ -22,8 +22,10 @@
 // into runs of key tiles merged by combine_kernel; prefill launches hand out
 // their unequal items longest first in zigzag rounds.  Warp roles (384 threads):
 //   warp 0      TMA producer: Q per item, then K0 V0 K1 V1 ... into a 5-stage ring
-//   warp 1      TMEM allocator; one thread issues tcgen05.mma, eight k-steps
-//               per asm block with every descriptor ready in registers
+//   warp 1      TMEM allocator and MMA issuer: the whole warp runs the issue
+//               loop in step (every wait is a warp vote), and one lane chosen
+//               by elect.sync issues each tcgen05.mma and tcgen05.commit; eight
+//               k-steps per asm block with every descriptor ready in registers
 //   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: thread = row
 //   warps 2-3   idle
 // Tensor memory (512 columns x 128 lanes): O0 [0,128) O1 [128,256)
@@ -31,7 +33,7 @@
 // and feeds the P V product straight from tensor memory.
 // MMA order per key tile j: PV0(j) QK0(j+1) PV1(j) QK1(j+1), so the softmax of
 // one tile overlaps the tensor-core work of the other.  A tcgen05.commit
-// completes only when every earlier MMA of the issuing thread has completed,
+// completes only when every earlier MMA issued from the warp has completed,
 // so when S(j+1) of tile w is ready, PV(j) of tile w is done and the softmax
 // threads may rescale O in place.  The reference max of a row moves only when
 // the running max grows by more than 2^8 (then O and l are rescaled); every
@@ -41,7 +43,7 @@
 // Every mbarrier wait is bounded (globaltimer).  A wait that runs out sets a
 // CTA-wide abort flag and the device error word; all roles then leave their
 // loops, the producer waits (bounded) for its copies in flight, the MMA
-// thread for its MMAs, and tensor memory is freed before the CTA exits.
+// warp for its MMAs, and tensor memory is freed before the CTA exits.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -176,8 +178,12 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+// commit from one elected lane of a converged warp
+__device__ __forceinline__ void tc_commit_e(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
+      : "memory");
 }
 #define LL_R8(i) "=r"(r[i + 0]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
                  "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
@@ -248,45 +254,47 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return r;
 }
 
-// Eight (or four) MMAs of one group from a single asm block: k-step 0 accumulates
-// when acc != 0, the others always.  D(tmem) (+)= A(smem) * B(smem)
+// Eight (or four) MMAs of one group from a single asm block, issued by the lane
+// that elect.sync picks (the whole warp executes the block; operands are the
+// same in every lane): k-step 0 accumulates when acc != 0, the others always.
+// D(tmem) (+)= A(smem) * B(smem)
 __device__ __forceinline__ void mma8_ss(uint32_t d, const uint64_t (&a)[8], const uint64_t (&b)[8], uint32_t idesc,
                                         uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p0, p1;\n\tsetp.ne.b32 p0, %18, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %1, p0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %1, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %1, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %1, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %1, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %1, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %1, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %17, %1, p1;\n\t}" ::"r"(d),
+      "{\n\t.reg .pred p0, p1, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p0, %18, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %1, p0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %1, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %1, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %1, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %1, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %1, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %1, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %9, %17, %1, p1;\n\t}" ::"r"(d),
       "r"(idesc), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]),
       "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(acc));
 }
 __device__ __forceinline__ void mma4_ss(uint32_t d, const uint64_t (&a)[4], const uint64_t (&b)[4], uint32_t idesc,
                                         uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p0, p1;\n\tsetp.ne.b32 p0, %10, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %1, p0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %1, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %1, p1;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %9, %1, p1;\n\t}" ::"r"(d),
+      "{\n\t.reg .pred p0, p1, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p0, %10, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %1, p0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %1, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %1, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %9, %1, p1;\n\t}" ::"r"(d),
       "r"(idesc), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc));
 }
 // D(tmem) (+)= A(tmem: 8 k-steps of 8 columns from column a) * B(smem)
 __device__ __forceinline__ void mma8_ts(uint32_t d, uint32_t a, const uint64_t (&b)[8], uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p0, p1;\n\t.reg .b32 t;\n\tsetp.ne.b32 p0, %11, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %3, %1, p0;\n\t"
-      "add.u32 t, %2, 8;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [t], %4, %1, p1;\n\t"
-      "add.u32 t, %2, 16;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [t], %5, %1, p1;\n\t"
-      "add.u32 t, %2, 24;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [t], %6, %1, p1;\n\t"
-      "add.u32 t, %2, 32;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [t], %7, %1, p1;\n\t"
-      "add.u32 t, %2, 40;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [t], %8, %1, p1;\n\t"
-      "add.u32 t, %2, 48;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [t], %9, %1, p1;\n\t"
-      "add.u32 t, %2, 56;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [t], %10, %1, p1;\n\t}" ::"r"(d),
+      "{\n\t.reg .pred p0, p1, e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .b32 t;\n\tsetp.ne.b32 p0, %11, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %3, %1, p0;\n\t"
+      "add.u32 t, %2, 8;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], %4, %1, p1;\n\t"
+      "add.u32 t, %2, 16;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], %5, %1, p1;\n\t"
+      "add.u32 t, %2, 24;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], %6, %1, p1;\n\t"
+      "add.u32 t, %2, 32;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], %7, %1, p1;\n\t"
+      "add.u32 t, %2, 40;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], %8, %1, p1;\n\t"
+      "add.u32 t, %2, 48;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], %9, %1, p1;\n\t"
+      "add.u32 t, %2, 56;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], %10, %1, p1;\n\t}" ::"r"(d),
       "r"(idesc), "r"(a), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
       "r"(acc));
 }
@@ -519,14 +527,18 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------ MMA issuer --------------------------------
+    {
+      // ------------------------------ MMA issuer (whole warp) --------------------
       constexpr uint32_t kIdQK = idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
       constexpr uint32_t kIdPV = idesc_bf16(BM, D, 0, 1);   // P from TMEM; V is N(=d)-major
-      // The tensor core takes one 128x128x16 MMA per 64 clocks, but this thread
+      // The tensor core takes one 128x128x16 MMA per 64 clocks, but this warp
       // shares its SMSP's issue slots with two busy softmax warps and gets few of
-      // them, so each MMA group must cost it as few instructions as possible:
-      // all operands are ready in registers and the eight MMAs of a group go out
+      // them, so each MMA group must cost it as few instructions as possible.
+      // All 32 lanes run this loop in step: every wait is a warp vote and the
+      // MMAs and commits go out under an elect.sync predicate, so the control
+      // flow and every descriptor are visibly warp-uniform (one lane alone
+      // behind a lane test measured 10 % slower over the whole kernel).  All
+      // operands are ready in registers and the eight MMAs of a group go out
       // from one asm block.  The Q descriptors of both query tiles and the
       // tensor-memory addresses of P are built once; the descriptors of a K or V
       // tile differ from the ring's first stage only in the start address field
@@ -568,44 +580,44 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       bool ok = true;
       while (ok && walker_next(wk, p, pc, blockIdx.x)) {
         const int n = pc.j1 - pc.j0;
-        if (!(ok = wait(bQfull, qi & 1, ctl))) break;
-        if (!(ok = wait(bKVfull0 + 8 * (u % NS), (u / NS) & 1, ctl))) break;
+        if (!(ok = __all_sync(0xffffffffu, wait(bQfull, qi & 1, ctl)))) break;
+        if (!(ok = __all_sync(0xffffffffu, wait(bKVfull0 + 8 * (u % NS), (u / NS) & 1, ctl)))) break;
         tc_fence_after();
         issue_qk(0, u % NS);
-        tc_commit(bS0);
+        tc_commit_e(bS0);
         issue_qk(1, u % NS);
-        tc_commit(bS0 + 8);
-        tc_commit(bKVempty0 + 8 * (u % NS));
-        if (n == 1) tc_commit(bQempty);
+        tc_commit_e(bS0 + 8);
+        tc_commit_e(bKVempty0 + 8 * (u % NS));
+        if (n == 1) tc_commit_e(bQempty);
         for (int t = 0; t < n; ++t) {
           const int uv = u + 2 * t + 1, sv = uv % NS;
           const int uk = u + 2 * t + 2, sk = uk % NS;
           const bool more = t + 1 < n;
-          if (!(ok = wait(bKVfull0 + 8 * sv, (uv / NS) & 1, ctl))) break;
-          if (!(ok = wait(bP0, (jt + t) & 1, ctl))) break;
+          if (!(ok = __all_sync(0xffffffffu, wait(bKVfull0 + 8 * sv, (uv / NS) & 1, ctl)))) break;
+          if (!(ok = __all_sync(0xffffffffu, wait(bP0, (jt + t) & 1, ctl)))) break;
           // the previous item's epilogue must have read O out of tensor memory
-          if (t == 0 && qi > 0 && !(ok = wait(bOempty, (qi - 1) & 1, ctl))) break;
+          if (t == 0 && qi > 0 && !(ok = __all_sync(0xffffffffu, wait(bOempty, (qi - 1) & 1, ctl)))) break;
           tc_fence_after();
           issue_pv(0, sv, t > 0);
           if (more) {
-            if (!(ok = wait(bKVfull0 + 8 * sk, (uk / NS) & 1, ctl))) break;
+            if (!(ok = __all_sync(0xffffffffu, wait(bKVfull0 + 8 * sk, (uk / NS) & 1, ctl)))) break;
             tc_fence_after();
             issue_qk(0, sk);
-            tc_commit(bS0);
+            tc_commit_e(bS0);
           }
-          if (!(ok = wait(bP0 + 8, (jt + t) & 1, ctl))) break;
+          if (!(ok = __all_sync(0xffffffffu, wait(bP0 + 8, (jt + t) & 1, ctl)))) break;
           tc_fence_after();
           issue_pv(1, sv, t > 0);
-          tc_commit(bKVempty0 + 8 * sv);
+          tc_commit_e(bKVempty0 + 8 * sv);
           if (more) {
             issue_qk(1, sk);
-            tc_commit(bS0 + 8);
-            tc_commit(bKVempty0 + 8 * sk);
-            if (t + 2 == n) tc_commit(bQempty);
+            tc_commit_e(bS0 + 8);
+            tc_commit_e(bKVempty0 + 8 * sk);
+            if (t + 2 == n) tc_commit_e(bQempty);
           }
         }
         if (!ok) break;
-        tc_commit(bOfull);
+        tc_commit_e(bOfull);
         u += 2 * n;
         jt += n;
         ++qi;
@@ -782,9 +794,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     const int first = tiles_issued > NS ? tiles_issued - NS : 0;
     for (int u = first; u < tiles_issued; ++u) wait_drain(bKVfull0 + 8 * (u % NS), (u / NS) & 1);
   }
-  if (warp == 1 && lane == 0) {
-    tc_commit(bDrain);
+  if (warp == 1) {
+    // a commit tracks the MMAs of its own thread: the lane elect.sync picks,
+    // as for every MMA and commit of the issue loop
+    tc_commit_e(bDrain);
     wait_drain(bDrain, 0);
+    __syncwarp();
   }
   tc_fence_before();
   __syncthreads();
