@@ -32,7 +32,11 @@
 // S0 [256,384) S1 [384,512).  P (bf16) overwrites the first 64 columns of S
 // and feeds the P V product straight from tensor memory.
 // MMA order per key tile j: PV0(j) QK0(j+1) PV1(j) QK1(j+1), so the softmax of
-// one tile overlaps the tensor-core work of the other.  A tcgen05.commit
+// one tile overlaps the tensor-core work of the other.  P of a tile is handed
+// over in two halves: once the P of keys 0-63 is in tensor memory the softmax
+// threads signal it and the tensor core starts P V on those four k-steps while
+// the exponentials of keys 64-127 run (a tile whose O must be rescaled signals
+// both halves at the end, after the rescale).  A tcgen05.commit
 // completes only when every earlier MMA issued from the warp has completed,
 // so when S(j+1) of tile w is ready, PV(j) of tile w is done and the softmax
 // threads may rescale O in place.  The reference max of a row moves only when
@@ -283,20 +287,17 @@ __device__ __forceinline__ void mma4_ss(uint32_t d, const uint64_t (&a)[4], cons
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %9, %1, p1;\n\t}" ::"r"(d),
       "r"(idesc), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc));
 }
-// D(tmem) (+)= A(tmem: 8 k-steps of 8 columns from column a) * B(smem)
-__device__ __forceinline__ void mma8_ts(uint32_t d, uint32_t a, const uint64_t (&b)[8], uint32_t idesc, uint32_t acc) {
+
+// D(tmem) (+)= A(tmem: 4 k-steps of 8 columns from column a) * B(smem), elected lane
+__device__ __forceinline__ void mma4_ts(uint32_t d, uint32_t a, const uint64_t (&b)[4], uint32_t idesc, uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p0, p1, e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .b32 t;\n\tsetp.ne.b32 p0, %11, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+      "{\n\t.reg .pred p0, p1, e;\n\t.reg .b32 t;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p0, %7, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %3, %1, p0;\n\t"
       "add.u32 t, %2, 8;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], %4, %1, p1;\n\t"
       "add.u32 t, %2, 16;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], %5, %1, p1;\n\t"
-      "add.u32 t, %2, 24;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], %6, %1, p1;\n\t"
-      "add.u32 t, %2, 32;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], %7, %1, p1;\n\t"
-      "add.u32 t, %2, 40;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], %8, %1, p1;\n\t"
-      "add.u32 t, %2, 48;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], %9, %1, p1;\n\t"
-      "add.u32 t, %2, 56;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], %10, %1, p1;\n\t}" ::"r"(d),
-      "r"(idesc), "r"(a), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
-      "r"(acc));
+      "add.u32 t, %2, 24;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], %6, %1, p1;\n\t}" ::"r"(d),
+      "r"(idesc), "r"(a), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc));
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
@@ -443,10 +444,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
   const uint32_t bKVempty0 = bKVfull0 + 8 * NS;
   const uint32_t bS0 = bKVempty0 + 8 * NS;
   const uint32_t bP0 = bS0 + 16;
-  const uint32_t bOfull = bP0 + 16;
+  const uint32_t bOfull = bP0 + 32;  // bP0: P of keys 0-63 of tile w at +8w, of keys 64-127 at +16+8w
   const uint32_t bOempty = bOfull + 8;
   const uint32_t bDrain = bOempty + 8;
-  constexpr int kBarBytes = 16 + 16 * NS + 16 + 16 + 24;
+  constexpr int kBarBytes = 16 + 16 * NS + 16 + 32 + 24;
   static_assert(kBarBytes + 8 <= 256, "barrier area");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Cf::kSmemBar + kBarBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Cf::kSmemBar + kBarBytes + 4);
@@ -465,6 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     for (int w = 0; w < NQ; ++w) {
       mbar_init(bS0 + 8 * w, 1);
       mbar_init(bP0 + 8 * w, 128);
+      mbar_init(bP0 + 16 + 8 * w, 128);
     }
     mbar_init(bOfull, 1);
     mbar_init(bOempty, NQ * 128);
@@ -566,12 +568,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         else
           mma4_ss(tmem + 256 + 128 * w, dq[w], bd, kIdQK, 0u);
       };
-      auto issue_pv = [&](int w, int stage, bool acc) {
+      // P V in two groups of four k-steps: keys 0-63, then keys 64-127
+      auto issue_pv = [&](int w, int stage, int half, bool acc) {
         const uint32_t lo = v_lo0 + (((uint32_t)stage * Cf::kTileBytes) >> 4);
-        uint64_t bd[BN / 16];
+        uint64_t bd[4];
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) bd[ks] = make_desc(lo + (ks * 16 * 128) / 16, v_hi);
-        mma8_ts(tmem + 128 * w, tmem + 256 + 128 * w, bd, kIdPV, acc ? 1u : 0u);
+        for (int ks = 0; ks < 4; ++ks) bd[ks] = make_desc(lo + ((half * 4 + ks) * 16 * 128) / 16, v_hi);
+        mma4_ts(tmem + 128 * w, tmem + 256 + 128 * w + 32 * half, bd, kIdPV, acc ? 1u : 0u);
       };
       Walker wk;
       walker_init(wk, p, blockIdx.x);
@@ -598,7 +601,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
           // the previous item's epilogue must have read O out of tensor memory
           if (t == 0 && qi > 0 && !(ok = __all_sync(0xffffffffu, wait(bOempty, (qi - 1) & 1, ctl)))) break;
           tc_fence_after();
-          issue_pv(0, sv, t > 0);
+          issue_pv(0, sv, 0, t > 0);
+          if (!(ok = __all_sync(0xffffffffu, wait(bP0 + 16, (jt + t) & 1, ctl)))) break;
+          tc_fence_after();
+          issue_pv(0, sv, 1, true);
           if (more) {
             if (!(ok = __all_sync(0xffffffffu, wait(bKVfull0 + 8 * sk, (uk / NS) & 1, ctl)))) break;
             tc_fence_after();
@@ -607,7 +613,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
           }
           if (!(ok = __all_sync(0xffffffffu, wait(bP0 + 8, (jt + t) & 1, ctl)))) break;
           tc_fence_after();
-          issue_pv(1, sv, t > 0);
+          issue_pv(1, sv, 0, t > 0);
+          if (!(ok = __all_sync(0xffffffffu, wait(bP0 + 24, (jt + t) & 1, ctl)))) break;
+          tc_fence_after();
+          issue_pv(1, sv, 1, true);
           tc_commit_e(bKVempty0 + 8 * sv);
           if (more) {
             issue_qk(1, sk);
@@ -632,7 +641,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     const uint32_t tS = tmem + lane_off + 256 + 128 * w;
     const uint32_t tO = tmem + lane_off + 128 * w;
     const uint32_t bS = bS0 + 8 * w;
-    const uint32_t bP = bP0 + 8 * w;
+    const uint32_t bP = bP0 + 8 * w;        // P of keys 0-63 stored
+    const uint32_t bP2 = bP0 + 16 + 8 * w;  // P of keys 64-127 stored
     const float sl2 = a.scale_log2;
     Walker wk;
     walker_init(wk, p, blockIdx.x);
@@ -706,6 +716,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
             add_bf16x2(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], pk[i]);
           }
           tmem_st16(tS + 16 * g, pk);
+          if (g == 1 && !rescale) {
+            // keys 0-63: their P is in tensor memory and O needs no rescale, so
+            // the tensor core may start on them (rescale is warp-uniform)
+            tmem_st_wait();
+            tc_fence_before();
+            if (!(a.stall_inject && jt + t == 0 && w == 0)) mbar_arrive(bP);
+          }
         }
         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         if (rescale) {
@@ -723,7 +740,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         }
         tmem_st_wait();
         tc_fence_before();
-        if (!(a.stall_inject && jt + t == 0 && w == 0)) mbar_arrive(bP);
+        if (!(a.stall_inject && jt + t == 0 && w == 0)) {
+          if (rescale) mbar_arrive(bP);
+          mbar_arrive(bP2);
+        }
       }
       if (!ok) break;
       ok = __all_sync(0xffffffffu, wait(bOfull, qi & 1, ctl));
