@@ -224,12 +224,27 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(power) if power else None}
 
 
-def kernel_source_hash():
+def code_hash(texts):
+    """Hash of C++/CUDA source texts with // comments, trailing blanks and blank lines removed,
+    so that an edit to comments alone leaves it unchanged (the sources hold no // inside a
+    string literal and no block comments)."""
     h = hashlib.sha256()
-    for f in ("ll_attend_tc.cu", "ll_internal.h"):
-        with open(os.path.join(ROOT, "windowed_sink_attention_ll_b300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    for text in texts:
+        for line in text.splitlines():
+            code = line.split("//", 1)[0].rstrip()
+            if code:
+                h.update(code.encode() + b"\n")
+        h.update(b"\0")
     return h.hexdigest()[:16]
+
+
+def kernel_source_hash():
+    """Code hash of the attention kernel's sources (ll_attend_tc.cu + ll_internal.h)."""
+    texts = []
+    for f in ("ll_attend_tc.cu", "ll_internal.h"):
+        with open(os.path.join(ROOT, "windowed_sink_attention_ll_b300", "csrc", f)) as fh:
+            texts.append(fh.read())
+    return code_hash(texts)
 
 
 def attend_bytes(shape: llsynth.Shape, resident_frames: int):

@@ -6,6 +6,7 @@ from the oracle's own visibility masks and commit bookkeeping, for the default
 reading and for the two options.
 """
 
+import os
 import sys
 
 import numpy as np
@@ -75,3 +76,27 @@ def test_stream_plan_matches_visible_frames():
     # steady state: 0.6728 TFLOP per attend launch of the Wan-shaped layer
     flops = bench.pair_flops(bench.chunk_pairs(s, 12, "chunk"), s.heads, s.head_dim)
     assert abs(flops - 0.672841728e12) < 1.0
+
+
+def test_code_hash_ignores_comments_only():
+    """The traffic record is keyed by a hash of the kernel's code: comment and blank-line
+    edits keep it, any change to the code changes it."""
+    src = "int f(int x) {  // doubles x\n  return 2 * x;\n}\n"
+    base = bench.code_hash([src, "#define N 4\n"])
+    assert bench.code_hash(["// header\n\n" + src.replace("doubles x", "twice x") + "\n\n",
+                            "#define N 4  // four\n"]) == base
+    assert bench.code_hash([src.replace("2 * x", "3 * x"), "#define N 4\n"]) != base
+    assert bench.code_hash([src, "#define N 5\n"]) != base
+    # file boundaries count: moving a line from one file to the next changes the hash
+    assert bench.code_hash([src + "#define N 4\n", ""]) != base
+
+
+def test_traffic_record_names_a_code_hash():
+    rec = {}
+    with open(os.path.join(ROOT, "profiles", "attend_tc_traffic.txt")) as f:
+        for line in f:
+            if "=" in line and not line.lstrip().startswith("#"):
+                k, v = line.split("=", 1)
+                rec[k.strip()] = v.strip()
+    assert len(rec["source_hash"]) == 16 and int(rec["source_hash"], 16) >= 0
+    assert float(rec["dram_bytes_per_launch"]) > float(rec["algorithmic_bytes_per_launch"]) > 0

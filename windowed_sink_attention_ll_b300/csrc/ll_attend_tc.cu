@@ -24,8 +24,10 @@
 //   warp 0      TMA producer: Q per item, then K0 V0 K1 V1 ... into a 5-stage ring
 //   warp 1      TMEM allocator and MMA issuer: the whole warp runs the issue
 //               loop in step (every wait is a warp vote), and one lane chosen
-//               by elect.sync issues each tcgen05.mma and tcgen05.commit; eight
-//               k-steps per asm block with every descriptor ready in registers
+//               by elect.sync issues each tcgen05.mma and tcgen05.commit; the
+//               eight k-steps of a Q K^T product go out from one asm block, a
+//               P V product from two blocks of four (one per key half), with
+//               every descriptor ready in registers
 //   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: thread = row
 //   warps 2-3   idle
 // Tensor memory (512 columns x 128 lanes): O0 [0,128) O1 [128,256)
