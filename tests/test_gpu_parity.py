@@ -346,3 +346,24 @@ def test_long_window_many_keys(ll):
     st.check_state()
     st.check_raw(0)
     st.close()
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_many_heads_split_tail(ll, D):
+    """64 heads of 200-token frames: 64 x 3 = 192 work items of 256 query rows, more than
+    the SMs, so an attend launch runs a whole round and then splits the left-over items;
+    every row of every pass checked against the oracle, state and slot bytes bit-exact."""
+    H, T, S, W, C = 64, 200, 2, 4, 3
+    st = Lockstep(ll, 1, H, D, T, S, W, C, torch.bfloat16)
+    L = C * T
+    for c in range(4):
+        q, k, v = (llsynth.seeded_normal(("many-heads", D, c, t), (L, H, D), device="cuda") for t in "qkv")
+        st.attend(0, q, k, v, commit=True, what="many heads d%d chunk %d" % (D, c))
+        st.check_state()
+    st.check_raw(0)
+    R = len(st.orc.recache_frames(0))
+    qw, kw, vw = (llsynth.seeded_normal(("many-heads-rc", D, t), (R * T, H, D), device="cuda") for t in "qkv")
+    st.recache_attend(0, qw, kw, vw, what="many heads d%d prefill" % D)
+    st.check_state()
+    st.check_raw(0)
+    st.close()
