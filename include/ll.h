@@ -240,12 +240,14 @@ LL_API ll_status ll_debug_use_simt(ll_cache* cache, int enable);
  * whole rounds, then the left-over items split into runs of key tiles),
  * mode 1 = recache prefill (La cached keys all visible, the Lb fresh keys
  * block-causal in blocks of block_tokens; persistent, items longest first in
- * zigzag rounds, none split).  Writes the
+ * zigzag rounds, none split), mode 2 = frame-causal chunk attend (the mode 0
+ * schedule; its mask is applied inside the tiles).  Writes the
  * CTA count to *grid, the pieces of work as (cta, item, first key tile, end key
  * tile, partial, scratch slot) sextuples into pieces[cap], and the items split
  * across CTAs as (item, parts, slot of each part ...) into splits[split_cap]
  * (*split_ints = ints written).  Returns the number of pieces (-1 on bad
- * arguments).  Items are (head, 256-row query block): head-major in mode 0,
+ * arguments: a size below 1, a mode other than 0-2, block_tokens < 1 in
+ * modes 1 and 2).  Items are (head, 256-row query block): head-major in mode 0,
  * last query block first in mode 1; key tiles hold 128 keys.
  */
 LL_API int ll_debug_attend_schedule(int Lq, int La, int Lb, int heads, int max_ctas, int mode, int block_tokens,

@@ -109,3 +109,93 @@ def test_prefill_schedule_covers_every_item_once_and_balances(ll, shape):
         mean = sum(load.values()) / grid
         longest = max(j for _, _, _, j, _, _ in pieces)
         assert max(load.values()) <= mean + longest
+
+
+def _check_attend(grid, pieces, splits, Lq, La, Lb, H, max_ctas):
+    nqb = -(-Lq // 256)
+    items = nqb * H
+    nkv = -(-La // 128) + -(-Lb // 128)
+    assert grid == min(max_ctas, 256, items)
+    seen = collections.Counter()
+    load = collections.Counter()
+    part_slots = {}
+    for cta, item, j0, j1, partial, slot in pieces:
+        assert 0 <= cta < grid and 0 <= item < items and 0 <= j0 < j1 <= nkv
+        for j in range(j0, j1):
+            seen[(item, j)] += 1
+        load[cta] += j1 - j0
+        assert partial == (0 if (j0 == 0 and j1 == nkv) else 1)
+        if partial:
+            assert slot in (2 * cta, 2 * cta + 1) and slot not in part_slots
+            part_slots[slot] = item
+    assert len(seen) == items * nkv and set(seen.values()) == {1}
+    by_item = collections.defaultdict(list)
+    for slot, item in part_slots.items():
+        by_item[item].append(slot)
+    assert {i: sorted(s) for i, s in by_item.items()} == {i: sorted(s) for i, s in splits}
+    assert all(len(s) >= 2 for _, s in splits)
+    # whole rounds first: every CTA carries rounds * nkv tiles before the tail
+    rounds, rem = divmod(items, grid)
+    tail = rem * nkv
+    # the tail goes to as many CTAs as runs of at least 16 tiles allow (all of them when
+    # the tail is long): those CTAs differ by at most one tile, the others carry no tail
+    tail_ctas = max(1, min(grid, tail // 16)) if tail else 0
+    loads = [load[c] for c in range(grid)]
+    assert min(loads) >= rounds * nkv
+    assert sum(loads) == items * nkv
+    if tail_ctas == grid:
+        assert max(loads) - min(loads) <= 1
+    elif tail:
+        assert max(loads) - min(loads) <= -(-tail // tail_ctas)
+
+
+def test_random_attend_schedules():
+    import numpy as np
+    import windowed_sink_attention_ll_b300 as ll
+
+    build_lib.build()
+    rng = np.random.default_rng(7)
+    for _ in range(300):
+        Lq = int(rng.integers(1, 12000))
+        La = int(rng.choice([0, int(rng.integers(1, 60000))]))
+        H = int(rng.integers(1, 25))
+        max_ctas = int(rng.choice([1, 2, 3, 7, 64, 148, 160, 300]))
+        shape = (Lq, La, Lq, H, max_ctas)
+        grid, pieces, splits = ll.ll_debug_attend_schedule(*shape)
+        _check_attend(grid, pieces, splits, *shape)
+        # the frame-causal chunk (mode 2) runs the attend schedule unchanged
+        block = int(rng.integers(1, Lq + 1))
+        assert ll.ll_debug_attend_schedule(*shape, mode=2, block_tokens=block) == (grid, pieces, splits), shape
+
+
+def test_random_prefill_schedules():
+    import numpy as np
+    import windowed_sink_attention_ll_b300 as ll
+
+    build_lib.build()
+    rng = np.random.default_rng(11)
+    for _ in range(200):
+        Lq = int(rng.integers(1, 20000))
+        La = int(rng.choice([0, int(rng.integers(1, 10000))]))
+        block = int(rng.integers(1, Lq + 1))
+        H = int(rng.integers(1, 25))
+        max_ctas = int(rng.choice([1, 3, 64, 148, 300]))
+        grid, pieces, splits = ll.ll_debug_attend_schedule(Lq, La, Lq, H, max_ctas, mode=1, block_tokens=block)
+        nqb = -(-Lq // 256)
+        items = nqb * H
+        assert grid == min(max_ctas, items) and splits == []
+        seen = collections.Counter()
+        load = collections.Counter()
+        for cta, item, j0, j1, partial, slot in pieces:
+            assert 0 <= cta < grid and 0 <= item < items and j0 == 0 and partial == 0
+            qb = nqb - 1 - item // H
+            last_row = min(Lq, (qb + 1) * 256) - 1
+            kv_end = min(Lq, (last_row // block + 1) * block)
+            assert j1 == -(-La // 128) + -(-kv_end // 128), (Lq, La, block, H, max_ctas, item)
+            seen[item] += 1
+            load[cta] += j1
+        assert len(seen) == items and set(seen.values()) == {1}
+        if items > grid:
+            mean = sum(load.values()) / grid
+            longest = max(p[3] for p in pieces)
+            assert max(load.values()) <= mean + longest

@@ -310,7 +310,8 @@ def ll_set_recache_scope(cache: LLCache, scope) -> None:
 
 def ll_debug_attend_schedule(Lq: int, La: int, Lb: int, heads: int, max_ctas: int, mode: int = 0,
                              block_tokens: int = 1):
-    """Host replay of a tensor-core attend (mode 0) or prefill (mode 1) launch's schedule (see include/ll.h).
+    """Host replay of a tensor-core attend (mode 0), prefill (mode 1) or frame-causal chunk (mode 2)
+    launch's schedule (see include/ll.h).
 
     Returns (grid, pieces, splits): pieces = list of (cta, item, j0, j1, partial,
     slot); splits = list of (item, [slots of its parts]).

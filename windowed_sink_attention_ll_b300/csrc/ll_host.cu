@@ -546,8 +546,8 @@ ll_status ll_profile_read(ll_cache* c, int kind, int64_t* launches, double* tota
 int ll_debug_attend_schedule(int Lq, int La, int Lb, int heads, int max_ctas, int mode, int block_tokens,
                              int* grid, int* pieces, int cap, int* splits, int split_cap, int* split_ints) {
   if (Lq < 1 || La < 0 || Lb < 1 || heads < 1 || max_ctas < 1 || !grid || !split_ints) return -1;
-  if (mode != 0 && mode != 1) return -1;
-  if (mode == 1 && block_tokens < 1) return -1;
+  if (mode < 0 || mode > 2) return -1;
+  if (mode != 0 && block_tokens < 1) return -1;
   return ll::attend_schedule_dump(Lq, La, Lb, heads, max_ctas, mode, block_tokens, grid, pieces, cap, splits,
                                   split_cap, split_ints);
 }
