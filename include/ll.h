@@ -75,8 +75,11 @@ LL_API const char* ll_status_str(ll_status s);
  * head-major [layer][head][slot][token][d].  The memory is cudaMalloc'ed on
  * the current device and zero-filled; ll_cache_destroy frees it.
  * Requirements: layers, heads, tokens_per_frame, chunk_frames >= 1;
- * sink_frames, window_frames >= 0; head_dim in {64, 128}.  Returns
- * LL_ERR_OOM if the allocation fails (then *out is NULL).
+ * sink_frames, window_frames >= 0; head_dim in {64, 128}.  Limits of this
+ * build, beyond which the call returns LL_ERR_UNSUPPORTED: S + W <= 512 and
+ * C <= 512 frames, heads <= 127 (the commit copy runs 512 x heads blocks at
+ * most), (S + W + C) * T <= 2^30 tokens.  Returns LL_ERR_OOM if the
+ * allocation fails.  On any error *out is NULL.
  */
 LL_API ll_status ll_cache_create(ll_cache** out, int layers, int heads, int head_dim,
                           int tokens_per_frame, int sink_frames, int window_frames,

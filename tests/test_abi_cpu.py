@@ -85,10 +85,33 @@ def test_create_rejects_bad_arguments_before_touching_a_device(ll):
         with pytest.raises(ll.LLError) as e:
             ll.ll_cache_create(*args)
         assert e.value.status == ll.LL_ERR_INVALID_ARG, args
-    for args in [(1, 2, 96, 16, 3, 6, 3, ll.LL_BF16), (1, 2, 64, 16, 400, 200, 3, ll.LL_BF16)]:
+    too_big = [
+        (1, 2, 96, 16, 3, 6, 3, ll.LL_BF16),         # head_dim not 64 / 128
+        (1, 2, 64, 16, 400, 200, 3, ll.LL_BF16),     # S + W = 600 > 512 frames
+        (1, 2, 64, 16, 3, 6, 513, ll.LL_BF16),       # C = 513 > 512 frames
+        (1, 128, 64, 16, 3, 6, 3, ll.LL_BF16),       # 128 heads > 127
+        (1, 2, 64, 1 << 27, 3, 6, 3, ll.LL_BF16),    # (S + W + C) * T = 12 * 2^27 > 2^30 tokens
+    ]
+    for args in too_big:
         with pytest.raises(ll.LLError) as e:
             ll.ll_cache_create(*args)
         assert e.value.status == ll.LL_ERR_UNSUPPORTED, args
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="at the limits a GPU would allocate")
+def test_create_limits_are_inclusive(ll):
+    # exactly at each limit the request passes every size check and stops at the
+    # device lookup (no GPU here)
+    at_limit = [
+        (1, 2, 64, 16, 500, 12, 3, ll.LL_BF16),      # S + W = 512
+        (1, 2, 64, 16, 3, 6, 512, ll.LL_BF16),       # C = 512
+        (1, 127, 64, 16, 3, 6, 3, ll.LL_BF16),       # 127 heads
+        (1, 2, 64, 1 << 26, 8, 5, 3, ll.LL_BF16),    # (S + W + C) * T = 16 * 2^26 = 2^30
+    ]
+    for args in at_limit:
+        with pytest.raises(ll.LLError) as e:
+            ll.ll_cache_create(*args)
+        assert e.value.status == ll.LL_ERR_CUDA, args
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-device path")
