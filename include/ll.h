@@ -129,6 +129,17 @@ LL_API ll_status ll_recache_attend(ll_cache* cache, int layer, const void* q_win
                             const void* v_win, void* out_win, void* stream);
 
 /*
+ * ll_recache_tokens -- the token rows that a recache of `layer` reads from
+ * k_win and v_win (and, for ll_recache_attend, from q_win and writes to
+ * out_win) in the cache's current state and recache scope: R * T, where R is
+ * the number of frames the recache rewrites (0 when it would return
+ * LL_ERR_STATE).  Host metadata only: no device work, no synchronisation.
+ * The recache calls take raw pointers and cannot see a buffer's length, so
+ * callers check theirs against this.
+ */
+LL_API ll_status ll_recache_tokens(const ll_cache* cache, int layer, int64_t* tokens);
+
+/*
  * ll_set_output_dtype -- element type of `out` / `out_win` in later calls.
  * Default: the cache dtype.  LL_FP32 on a bf16 cache returns the fp32
  * accumulator result unrounded (bf16 rounding alone costs up to |o| * 2^-9,

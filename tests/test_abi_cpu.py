@@ -132,6 +132,7 @@ def test_null_handle_calls_return_invalid_arg(ll):
     assert lib.ll_cache_read(None, 0, None, None) == ll.LL_ERR_INVALID_ARG
     assert lib.ll_cache_info(None, None, None, None) == ll.LL_ERR_INVALID_ARG
     assert lib.ll_debug_inject_stall(None, 1, 10) == ll.LL_ERR_INVALID_ARG
+    assert lib.ll_recache_tokens(None, 0, None) == ll.LL_ERR_INVALID_ARG
     lib.ll_cache_destroy(None)
 
 

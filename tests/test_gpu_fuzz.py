@@ -75,6 +75,7 @@ def test_random_call_sequence(ll, seed):
                 st.check_raw(layer)
         elif op in ("prefill", "recache"):
             R = len(st.orc.recache_frames(layer))
+            assert ll.ll_recache_tokens(st.cache, layer) == R * T, what
             if R == 0:
                 z = torch.zeros((T, H, D), dtype=dtype, device="cuda")
                 with pytest.raises(ll.LLError) as e:

@@ -147,6 +147,15 @@ def test_reset_and_empty_recache(ll):
         ll.ll_attend_chunk(st.cache, 2, q, k, v, torch.empty_like(q), True)
     assert e.value.status == ll.LL_ERR_INVALID_ARG
     st.check_state()
+    # a recache window of the wrong length is refused before the library reads it
+    assert ll.ll_recache_tokens(st.cache, 0) == 0
+    st.attend(0, q, k, v, commit=True, what="commit after reset")
+    assert ll.ll_recache_tokens(st.cache, 0) == 3 * 16
+    short = torch.zeros(2 * 16, 2, 64, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ValueError):
+        ll.ll_recache(st.cache, 0, short, short)
+    st.check_state()
+    st.check_raw(0)
     st.close()
 
 

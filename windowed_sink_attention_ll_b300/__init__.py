@@ -37,7 +37,7 @@ EXPORTS = ("ll_status_str", "ll_cache_create", "ll_cache_destroy", "ll_attend_ch
            "ll_cache_info", "ll_frame_slot", "ll_resident_frames", "ll_launch_count",
            "ll_debug_inject_stall", "ll_debug_use_simt", "ll_profile_enable", "ll_profile_read",
            "ll_set_output_dtype", "ll_debug_attend_schedule", "ll_attend_chunk_noalloc",
-           "ll_set_chunk_mask", "ll_set_recache_scope")
+           "ll_set_chunk_mask", "ll_set_recache_scope", "ll_recache_tokens")
 LL_KERNEL_ATTEND, LL_KERNEL_PREFILL, LL_KERNEL_COPY = 0, 1, 2
 LL_MASK_CHUNK, LL_MASK_FRAME = 0, 1
 LL_RECACHE_RESIDENT, LL_RECACHE_WINDOW = 0, 1
@@ -88,6 +88,7 @@ def _lib() -> ctypes.CDLL:
             "ll_attend_chunk_noalloc": (i32, [vp, vp, vp, i32, i64, vp, vp, i32, vp, i32, i32, vp, vp]),
             "ll_set_chunk_mask": (i32, [vp, i32]),
             "ll_set_recache_scope": (i32, [vp, i32]),
+            "ll_recache_tokens": (i32, [vp, i32, ctypes.POINTER(i64)]),
         }
         for name, (res, args) in sig.items():
             f = getattr(lib, name)
@@ -201,14 +202,30 @@ def ll_attend_chunk(cache: LLCache, layer: int, q, k, v, out, commit: bool, stre
            "ll_attend_chunk")
 
 
+def ll_recache_tokens(cache: LLCache, layer: int) -> int:
+    """Token rows a recache of `layer` reads now (R * T; 0 when the recache would be refused)."""
+    n = ctypes.c_int64()
+    _check(_lib().ll_recache_tokens(cache.ptr, layer, ctypes.byref(n)), "ll_recache_tokens")
+    return n.value
+
+
+def _recache_rows(cache: LLCache, layer: int, t, name: str) -> int:
+    """Rows of a recache window tensor, checked against what the library will read."""
+    L = t.shape[0] if isinstance(t, torch.Tensor) and t.dim() > 0 else -1
+    want = ll_recache_tokens(cache, layer)
+    if want and L != want:
+        raise ValueError("%s has %d token rows; a recache of layer %d reads %d" % (name, L, layer, want))
+    return L
+
+
 def ll_recache(cache: LLCache, layer: int, k_win, v_win, stream=None) -> None:
-    L = k_win.shape[0] if isinstance(k_win, torch.Tensor) else -1
+    L = _recache_rows(cache, layer, k_win, "k_win")
     _check(_lib().ll_recache(cache.ptr, layer, _ptr(cache, k_win, L, "k_win"), _ptr(cache, v_win, L, "v_win"),
                              _stream(stream)), "ll_recache")
 
 
 def ll_recache_attend(cache: LLCache, layer: int, q_win, k_win, v_win, out_win, stream=None) -> None:
-    L = q_win.shape[0] if isinstance(q_win, torch.Tensor) else -1
+    L = _recache_rows(cache, layer, q_win, "q_win")
     ptrs = [_ptr(cache, t, L, n) for t, n in ((q_win, "q_win"), (k_win, "k_win"), (v_win, "v_win"),
                                               (out_win, "out_win"))]
     _check(_lib().ll_recache_attend(cache.ptr, layer, *ptrs, _stream(stream)), "ll_recache_attend")

@@ -421,6 +421,16 @@ static ll_status recache_common(ll_cache* c, int layer, const void* q_win, const
   return launch_copy(c, layer, k_win, v_win, slot_of, st);
 }
 
+ll_status ll_recache_tokens(const ll_cache* c, int layer, int64_t* tokens) {
+  if (ll_status s = check_layer(c, layer)) return s;
+  if (!tokens) return LL_ERR_INVALID_ARG;
+  const int64_t n = c->n[layer];
+  int64_t R = resident_count(c->S, c->W, n);
+  if (c->recache_scope == LL_RECACHE_WINDOW) R -= n < c->S ? n : c->S;  // the sink keeps its K/V
+  *tokens = R * c->T;
+  return LL_OK;
+}
+
 ll_status ll_recache(ll_cache* c, int layer, const void* k_win, const void* v_win, void* stream) {
   return recache_common(c, layer, nullptr, k_win, v_win, nullptr, stream);
 }
