@@ -58,7 +58,7 @@ typedef enum { LL_BF16 = 0, LL_FP32 = 1 } ll_dtype;
 typedef enum {
   LL_OK = 0,
   LL_ERR_INVALID_ARG = 1,   /* bad shape, null or misaligned pointer, layer out of range */
-  LL_ERR_UNSUPPORTED = 2,   /* valid request this build does not implement (e.g. d not 64/128) */
+  LL_ERR_UNSUPPORTED = 2,   /* valid request the library does not implement (e.g. d not 64/128) */
   LL_ERR_OOM = 3,           /* device allocation failed in ll_cache_create */
   LL_ERR_STATE = 4,         /* call not allowed in the cache's state (e.g. recache of an empty layer) */
   LL_ERR_CUDA = 5,          /* a CUDA runtime call or kernel launch failed */
@@ -75,8 +75,8 @@ LL_API const char* ll_status_str(ll_status s);
  * head-major [layer][head][slot][token][d].  The memory is cudaMalloc'ed on
  * the current device and zero-filled; ll_cache_destroy frees it.
  * Requirements: layers, heads, tokens_per_frame, chunk_frames >= 1;
- * sink_frames, window_frames >= 0; head_dim in {64, 128}.  Limits of this
- * build, beyond which the call returns LL_ERR_UNSUPPORTED: S + W <= 512 and
+ * sink_frames, window_frames >= 0; head_dim in {64, 128}.  Limits of the
+ * library, beyond which the call returns LL_ERR_UNSUPPORTED: S + W <= 512 and
  * C <= 512 frames, heads <= 127 (the commit copy runs 512 x heads blocks at
  * most), (S + W + C) * T <= 2^30 tokens.  Returns LL_ERR_OOM if the
  * allocation fails.  On any error *out is NULL.

@@ -26,7 +26,7 @@ What the method computes (the plain definition this module writes out):
   §3.3 says the recache rebuilds the cache from the most recent frames.
 * §4.4 (Table 4) "no KV cache" strategy: clear the whole cache at a switch.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 
 * W counts preceding frames only; the chunk being generated is always visible
   in full to itself (chunk-level block causality).
