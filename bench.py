@@ -107,6 +107,8 @@ def pair_flops(pairs, H, d):
 def set_options(ll, cache, args):
     ll.ll_set_chunk_mask(cache, args.chunk_mask)
     ll.ll_set_recache_scope(cache, args.recache_scope)
+    if args.pair:
+        ll.ll_debug_pair_kernel(cache, True)
 
 
 def append_bytes(shape: llsynth.Shape, frames_written: int):
@@ -239,9 +241,9 @@ def code_hash(texts):
 
 
 def kernel_source_hash():
-    """Code hash of the attention kernel's sources (ll_attend_tc.cu + ll_internal.h)."""
+    """Code hash of the attention kernel's sources (ll_attend_tc.cu + ll_tc_common.cuh + ll_internal.h)."""
     texts = []
-    for f in ("ll_attend_tc.cu", "ll_internal.h"):
+    for f in ("ll_attend_tc.cu", "ll_tc_common.cuh", "ll_internal.h"):
         with open(os.path.join(ROOT, "windowed_sink_attention_ll_b300", "csrc", f)) as fh:
             texts.append(fh.read())
     return code_hash(texts)
@@ -371,6 +373,10 @@ def timed_region(args, world, local, caches, step, profile_every=1):
     return ev0.elapsed_time(ev1), clk.summary(), launches, prof
 
 
+def attend_kernel_name(args):
+    return "attend_pair_kernel (CTA pair)" if args.pair else "attend_tc_kernel<128>"
+
+
 def tensor_roofline(kernel, flops, n, ms, pk, pk_src, sustained=True):
     """Tensor-bound roofline object of one kernel: flops over its summed CUDA-event time."""
     achieved = flops / (ms / 1e3) / 1e12 if ms > 0 else 0.0
@@ -458,17 +464,20 @@ def run_ours(args, world, rank, local):
         "chunk_mask": args.chunk_mask, "recache_scope": args.recache_scope,
         "parallelism": "replicas x%d (independent streams, no collective)" % world}))
     result = base_result(args, world, step_frames * args.steps * world / (ms_max / 1e3), ms_max, config)
-    roof = tensor_roofline("attend_tc_kernel<128>", att_sampled, n_att, ms_att, pk, pk_src)
+    roof = tensor_roofline(attend_kernel_name(args), att_sampled, n_att, ms_att, pk, pk_src)
     roof["sampling"] = "one launch in ten of each kind bracketed with CUDA events in the timed region"
     alg = sum(attend_bytes(shape, resident_count(S, W, t0)) for t0, _ in plan) / len(plan)
     roof["algorithmic_bytes_per_launch"] = alg
-    roof["traffic"], src = traffic_per_launch(alg)
+    roof["traffic"], src = traffic_per_launch(alg) if not args.pair else (None, None)
     if src:
         roof["traffic_source"] = "ncu capture of %s, scaled by algorithmic bytes" % src
+    in_stream = hbm_roofline("copy_frames_kernel", cp_sampled, n_cp, ms_cp, pk)
+    in_stream["how"] = "one commit copy in ten bracketed singly with CUDA events inside the timed stream"
     result.update({
         "tflops": step_flops * args.steps * world / (ms_max / 1e3) / 1e12,
         "roofline": roof,
-        "append": hbm_roofline("copy_frames_kernel", cp_sampled, n_cp, ms_cp, pk),
+        "append": append_batch(ll, cache, shape, inputs, pk),
+        "append_in_stream_brackets": in_stream,
         "gpu_launches": launches,
         "clocks": clocks,
     })
@@ -481,6 +490,57 @@ def run_ours(args, world, rank, local):
         result["cpu_baseline"] = {"value": step_frames / (step_flops / rate), "unit": UNIT, "cores": threads,
                                   "kind": "oracle", "sample": sample}
     return result
+
+
+def append_batch(ll, cache, shape, inputs, pk, reps=5):
+    """HBM roofline of the commit copy, batch-timed.
+
+    Every layer of the 30-layer cache holds one committed chunk (the 3 sink frames), and
+    ll_recache then rewrites those 3 frames in every layer: the same copy kernel moving the
+    same bytes as a commit (3 frames x 12 heads x 1560 tokens x 128, K and V, read + write).
+    The 30 launches, on distinct layers and distinct source buffers (1.7 GB in all, well
+    above the 126 MB L2), are recorded once as a CUDA graph, so that host-side call overhead
+    does not starve the GPU, and each replay is timed between one pair of CUDA events: the
+    figure includes the DRAM write-back of each launch and the gaps between launches, but no
+    per-launch event overhead."""
+    layers = shape.layers
+    ll.ll_reset(cache)
+    for l in range(layers):
+        q, k, v = inputs[l][0]
+        ll.ll_attend_chunk(cache, l, q, k, v, torch.empty_like(q), True)
+    assert all(ll.ll_recache_tokens(cache, l) == shape.chunk_tokens for l in range(layers))
+    srcs = [inputs[l][1 + l % (len(inputs[l]) - 1)][1:] for l in range(layers)]
+
+    def batch():
+        st = torch.cuda.current_stream()
+        for l in range(layers):
+            ll.ll_recache(cache, l, *srcs[l], st)
+
+    batch()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    n0 = ll.ll_launch_count()
+    with torch.cuda.graph(g):
+        batch()
+    assert ll.ll_launch_count() - n0 == layers
+    stream = torch.cuda.current_stream()
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    nbytes = append_bytes(shape, shape.chunk_frames) * layers
+    roof = hbm_roofline("copy_frames_kernel", nbytes * reps, layers * reps, ms * reps, pk)
+    roof["how"] = ("30 commit-sized copies (one per layer, distinct buffers) recorded as one CUDA graph; each "
+                   "replay timed between one pair of CUDA events, median of %d replays" % reps)
+    return roof
 
 
 def run_graph(args, world, local, ll, cache, step, step_frames, step_flops, shape, L, chunks):
@@ -555,11 +615,11 @@ def run_single(args, world, rank, local):
     config.update(shape_config(shape, {"passes": passes, "l2": "8 distinct chunks cycled (1.4 GB of q/k/v)",
                                        "chunk_mask": args.chunk_mask}))
     result = base_result(args, world, C * args.steps * world / (ms_max / 1e3), ms_max, config)
-    roof = tensor_roofline("attend_tc_kernel<128>", pass_flops * passes * args.steps, n_att, ms_att, pk, pk_src,
+    roof = tensor_roofline(attend_kernel_name(args), pass_flops * passes * args.steps, n_att, ms_att, pk, pk_src,
                            sustained=False)
     alg = attend_bytes(shape, S + W)
     roof["algorithmic_bytes_per_launch"] = alg
-    roof["traffic"], src = traffic_per_launch(alg)
+    roof["traffic"], src = traffic_per_launch(alg) if not args.pair else (None, None)
     if src:
         roof["traffic_source"] = "ncu capture of %s" % src
     result.update({
@@ -625,8 +685,8 @@ def run_recache30(args, world, rank, local):
     result = base_result(args, world, chunks * C * args.steps * world / (ms_max / 1e3), ms_max, config)
     result.update({
         "tflops": (att_flops + step_pre_flops) * args.steps * world / (ms_max / 1e3) / 1e12,
-        "roofline": tensor_roofline("attend_tc_kernel<128>", att_flops * args.steps, n_att, ms_att, pk, pk_src),
-        "prefill": dict(tensor_roofline("attend_tc_kernel<128> (prefill mode)", step_pre_flops * args.steps, n_pre,
+        "roofline": tensor_roofline(attend_kernel_name(args), att_flops * args.steps, n_att, ms_att, pk, pk_src),
+        "prefill": dict(tensor_roofline(attend_kernel_name(args) + " (prefill mode)", step_pre_flops * args.steps, n_pre,
                                         ms_pre, pk, pk_src),
                         ms_per_switch_30_layers=ms_pre / max(1, args.steps * switches)),
         "gpu_launches": launches, "clocks": clocks,
@@ -803,6 +863,8 @@ def main():
                     help="chunk (default): a chunk sees all its frames; frame: the frame-causal reading")
     ap.add_argument("--recache-scope", choices=["resident", "window"], default="resident",
                     help="resident (default): recache rewrites sink and window; window: the sink keeps its K/V")
+    ap.add_argument("--pair", action="store_true",
+                    help="run head_dim 128 on the CTA-pair tensor-core kernel instead of the default one-CTA kernel")
     ap.add_argument("--ref-budget-s", type=float, default=None,
                     help="seconds of oracle work per step of the reference arm (default: sized so the run takes "
                          "about two minutes)")

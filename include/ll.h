@@ -248,6 +248,15 @@ LL_API ll_status ll_debug_inject_stall(ll_cache* cache, int enable, int timeout_
 LL_API ll_status ll_debug_use_simt(ll_cache* cache, int enable);
 
 /*
+ * Test hook: a non-zero value routes this cache's bf16 attention at head_dim 128
+ * through the CTA-pair tensor-core kernel (two SMs share every MMA, M = 256;
+ * slower than the default one-CTA kernel on B300) instead of the one-CTA
+ * kernel, so tests and benchmarks can run both on the same inputs.  Other
+ * head dims ignore it.
+ */
+LL_API ll_status ll_debug_pair_kernel(ll_cache* cache, int enable);
+
+/*
  * Test hook (host only, no device needed): replay the work schedule of a
  * tensor-core attention launch with Lq queries, La cached and Lb fresh keys
  * per head and at most max_ctas CTAs; mode 0 = chunk attend (persistent:
@@ -304,7 +313,8 @@ LL_API int ll_debug_attend_schedule(int Lq, int La, int Lb, int heads, int max_c
  * device array of LL_NOALLOC_SCRATCH_BYTES (37.6 MiB), which every GPU that
  * loads the library holds until the process exits: two partial results of 256
  * query rows per CTA for up to LL_NOALLOC_PARTIAL_SLOTS / 2 = 148 CTAs at
- * head_dim 128 (one per SM of a B300; 291 CTAs at head_dim 64).  A request that
+ * head_dim 128 (one per SM of a B300).  At head_dim 64 the array would hold
+ * 291 CTAs' partial results, but no attend launch uses more than 256 CTAs.  A request that
  * would need more (a GPU with more SMs and more work items than that) returns
  * LL_ERR_UNSUPPORTED before anything is enqueued; so do head_dim not in
  * {64, 128} and cached_tokens + chunk_tokens > 2^30.  Bad pointers, strides or

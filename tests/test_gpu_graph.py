@@ -2,14 +2,20 @@
 
 The library keeps its frame bookkeeping on the host and enqueues plain kernel
 launches, so a whole stream step from an empty cache (every layer, every chunk,
-each pass committing) can be recorded with torch.cuda.graph and replayed; the
-replay's outputs and raw cache bytes must equal an eager run's bit for bit.
+each pass committing) can be recorded with torch.cuda.graph and replayed
+("LongLive", §3.3 "Short window attention": the chunk-by-chunk streaming loop
+over the rolling sink + window cache).  The replay's outputs and raw cache bytes
+must equal an eager run's bit for bit, and the replayed outputs must match the
+float64 oracle driven through the same calls (sampled query rows, every layer
+and chunk, the usual bound: max |err| <= 1e-2, relative L2 <= 5e-3).
 """
 
 import pytest
 import torch
 
 import llsynth
+import oracle
+from tests.gpu_util import compare, f64, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -27,7 +33,7 @@ def ll():
 
 
 @pytest.mark.parametrize("mask", ["chunk", "frame"])
-def test_stream_replayed_from_a_cuda_graph_equals_eager(ll, mask):
+def test_stream_replayed_from_a_cuda_graph_equals_eager_and_oracle(ll, mask):
     layers, H, D, T, S, W, C, chunks = 2, 12, 128, 1040, 3, 6, 3, 6  # 156 items: split tail too
     L = C * T
     cache = ll.ll_cache_create(layers, H, D, T, S, W, C, ll.LL_BF16)
@@ -62,4 +68,17 @@ def test_stream_replayed_from_a_cuda_graph_equals_eager(ll, mask):
                 assert torch.equal(outs[l][c], eager[l][c]), (l, c)
             k, v = ll.ll_cache_read(cache, l)
             assert torch.equal(k, eager_raw[l][0]) and torch.equal(v, eager_raw[l][1]), l
+
+    # the replayed outputs against the oracle fed the same calls in the same order
+    orc = oracle.OracleCache(layers, H, D, T, S, W, C)
+    orc.set_chunk_mask(mask)
+    rows = sample_rows(L, 96, seed=7)
+    for c in range(chunks):
+        for l in range(layers):
+            q, k, v = (f64(t) for t in inputs[l][c])
+            want = orc.attend(l, q, k, v, True, rows=rows)
+            compare(outs[l][c][torch.as_tensor(rows, device="cuda")], want,
+                    "graph replay vs oracle, mask %s, layer %d chunk %d" % (mask, l, c))
+    for l in range(layers):
+        assert ll.ll_cache_state(cache, l) == orc.state(l), l
     cache.close()

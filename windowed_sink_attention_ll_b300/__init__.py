@@ -37,7 +37,7 @@ EXPORTS = ("ll_status_str", "ll_cache_create", "ll_cache_destroy", "ll_attend_ch
            "ll_cache_info", "ll_frame_slot", "ll_resident_frames", "ll_launch_count",
            "ll_debug_inject_stall", "ll_debug_use_simt", "ll_profile_enable", "ll_profile_read",
            "ll_set_output_dtype", "ll_debug_attend_schedule", "ll_attend_chunk_noalloc",
-           "ll_set_chunk_mask", "ll_set_recache_scope", "ll_recache_tokens")
+           "ll_set_chunk_mask", "ll_set_recache_scope", "ll_recache_tokens", "ll_debug_pair_kernel")
 LL_KERNEL_ATTEND, LL_KERNEL_PREFILL, LL_KERNEL_COPY = 0, 1, 2
 LL_MASK_CHUNK, LL_MASK_FRAME = 0, 1
 LL_RECACHE_RESIDENT, LL_RECACHE_WINDOW = 0, 1
@@ -79,6 +79,7 @@ def _lib() -> ctypes.CDLL:
             "ll_launch_count": (ctypes.c_uint64, []),
             "ll_debug_inject_stall": (i32, [vp, i32, i32]),
             "ll_debug_use_simt": (i32, [vp, i32]),
+            "ll_debug_pair_kernel": (i32, [vp, i32]),
             "ll_profile_enable": (i32, [vp, i32]),
             "ll_set_output_dtype": (i32, [vp, i32]),
             "ll_debug_attend_schedule": (i32, [i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32),
@@ -165,6 +166,8 @@ def _ptr(cache: LLCache, t, tokens: int, name: str) -> int:
         raise TypeError("%s must be a torch.Tensor" % name)
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor" % name)
+    if cache.device is not None and t.device.index != cache.device:
+        raise ValueError("%s is on cuda:%s; the cache lives on cuda:%d" % (name, t.device.index, cache.device))
     want = cache.out_dtype if name.startswith("out") else cache.torch_dtype
     if t.dtype != want:
         raise ValueError("%s has dtype %s, expected %s" % (name, t.dtype, want))
@@ -290,6 +293,11 @@ def ll_debug_use_simt(cache: LLCache, enable: bool) -> None:
     _check(_lib().ll_debug_use_simt(cache.ptr, 1 if enable else 0), "ll_debug_use_simt")
 
 
+def ll_debug_pair_kernel(cache: LLCache, enable: bool) -> None:
+    """head_dim 128 on the CTA-pair tensor-core kernel instead of the one-CTA kernel (test hook)."""
+    _check(_lib().ll_debug_pair_kernel(cache.ptr, 1 if enable else 0), "ll_debug_pair_kernel")
+
+
 def ll_profile_enable(cache: LLCache, enable, every: int = 1) -> None:
     """Time one launch in every `every` of each kind (enable=False: off)."""
     _check(_lib().ll_profile_enable(cache.ptr, max(1, int(every)) if enable else 0), "ll_profile_enable")
@@ -361,25 +369,34 @@ def ll_attend_chunk_noalloc(q, k_cached, v_cached, cached_tokens: int, k, v, out
     CUDA tensor of one element that a timed-out device wait sets to 1.
     """
     L, H, d = (tuple(q.shape) + (0, 0, 0))[:3]
+    # the library runs on the current device and encodes every pointer into that device's
+    # tensor maps, so every tensor must live there
+    dev = torch.cuda.current_device()
+
+    def on_dev(t):
+        return t.device.index == dev
+
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (out, "out")):
         if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()
-                and tuple(t.shape) == (L, H, d)):
-            raise ValueError("%s must be a contiguous bf16 CUDA tensor of shape %s" % (n, (L, H, d)))
+                and tuple(t.shape) == (L, H, d) and on_dev(t)):
+            raise ValueError("%s must be a contiguous bf16 tensor of shape %s on cuda:%d" % (n, (L, H, d), dev))
     kc = vc = None
     stride = 0
     if cached_tokens > 0:
         for t, n in ((k_cached, "k_cached"), (v_cached, "v_cached")):
             if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16 and t.dim() == 3
                     and t.shape[0] == H and t.shape[1] >= cached_tokens and t.shape[2] == d
-                    and t.stride(2) == 1 and t.stride(1) == d):
-                raise ValueError("%s must be a bf16 CUDA tensor [H, >= cached_tokens, d] with contiguous rows" % n)
+                    and t.stride(2) == 1 and t.stride(1) == d and on_dev(t)):
+                raise ValueError("%s must be a bf16 tensor [H, >= cached_tokens, d] with contiguous rows on cuda:%d"
+                                 % (n, dev))
         if k_cached.stride(0) != v_cached.stride(0):
             raise ValueError("k_cached and v_cached must have the same head stride")
         kc, vc, stride = k_cached.data_ptr(), v_cached.data_ptr(), k_cached.stride(0)
     ew = None
     if err_word is not None:
-        if not (isinstance(err_word, torch.Tensor) and err_word.is_cuda and err_word.dtype == torch.int32):
-            raise ValueError("err_word must be an int32 CUDA tensor")
+        if not (isinstance(err_word, torch.Tensor) and err_word.is_cuda and err_word.dtype == torch.int32
+                and err_word.numel() >= 1 and on_dev(err_word)):
+            raise ValueError("err_word must be an int32 tensor of at least one element on cuda:%d" % dev)
         ew = err_word.data_ptr()
     _check(_lib().ll_attend_chunk_noalloc(q.data_ptr(), kc, vc, cached_tokens, stride, k.data_ptr(), v.data_ptr(),
                                           L, out.data_ptr(), H, d, ew, _stream(stream)),

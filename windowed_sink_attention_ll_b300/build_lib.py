@@ -18,8 +18,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libll.so")
-SOURCES = ["ll_host.cu", "ll_copy_frames.cu", "ll_attend_simt.cu", "ll_attend_tc.cu", "ll_noalloc.cu"]
-HEADERS = [os.path.join(CSRC, "ll_internal.h"), os.path.join(ROOT, "include", "ll.h")]
+SOURCES = ["ll_host.cu", "ll_copy_frames.cu", "ll_attend_simt.cu", "ll_attend_tc.cu", "ll_attend_pair.cu",
+           "ll_noalloc.cu"]
+HEADERS = [os.path.join(CSRC, "ll_internal.h"), os.path.join(CSRC, "ll_tc_common.cuh"),
+           os.path.join(ROOT, "include", "ll.h")]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo", "-O3", "-std=c++17",
          "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden", "-cudart", "static",

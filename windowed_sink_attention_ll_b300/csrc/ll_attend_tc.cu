@@ -16,8 +16,11 @@
 // every cached key, and masks the chunk's own keys the same block-causal way
 // (the frame-causal chunk).
 //
+// This is the one-CTA form of the kernel, the one every bf16 attention runs on;
+// ll_attend_pair.cu holds a CTA-pair form for head_dim 128 (selected on request).
 // Work item = one head x 256 query rows (two 128-row tiles that share every
-// K/V tile); one CTA per SM walks several items (see "Work schedule"):
+// K/V tile); one CTA per SM walks several items (see "Work schedule" in
+// ll_tc_common.cuh):
 // attend launches run whole rounds of items, then split the left-over items
 // into runs of key tiles merged by combine_kernel; prefill launches hand out
 // their unequal items longest first in zigzag rounds.  Warp roles (384 threads):
@@ -50,26 +53,20 @@
 // CTA-wide abort flag and the device error word; all roles then leave their
 // loops, the producer waits (bounded) for its copies in flight, the MMA
 // warp for its MMAs, and tensor memory is freed before the CTA exits.
-#include <cuda.h>
-#include <cudaTypedefs.h>
-#include <cuda_bf16.h>
-
-#include <cstring>
-
-#include "ll_internal.h"
+#include "ll_tc_common.cuh"
 
 namespace ll {
 
 namespace {
 
+using namespace tc;
+
 constexpr int BM = 128;        // query rows per tile = TMEM lanes
-constexpr int BN = 128;        // keys per K/V tile
+constexpr int BN = kKeyTile;   // keys per K/V tile
 constexpr int NQ = 2;          // query tiles per CTA
 constexpr int NS = 5;          // stages of the K/V tile ring
 constexpr int kThreads = 384;
-constexpr int kAtom = 16384;   // one 128-row x 128-byte swizzled TMA box
-constexpr float kRescaleLog2 = 8.0f;
-constexpr long long kDrainNs = 200000000LL;  // 0.2 s for copies/MMAs already in flight
+static_assert(NQ * BM == kItemRows, "a CTA takes one work item");
 
 template <int D>
 struct Cfg {
@@ -84,95 +81,13 @@ struct Cfg {
 struct TcParams {
   CUtensorMap tm_q, tm_kc, tm_vc, tm_kn, tm_vn;
   AttendArgs a;
-  int nqb;               // query blocks of NQ * BM rows per head
-  int nkv;               // attend: key tiles per item
-  int grid;              // CTAs launched
-  int rounds;            // attend: whole-item rounds
-  int tail_ctas;         // attend: CTAs sharing the left-over items
-  long long tail_iters;  // attend: key tiles of the left-over items
-  float* part;           // scratch: partial O [2*grid][NQ*BM][D], then m and l [2*grid][NQ*BM] each
-};
-
-constexpr int kMaxSplit = 256;  // most CTAs of a persistent attend launch
-
-struct CombineParams {
-  void* out;
-  const float* part;
-  int grid;  // the attend launch's CTAs; scratch slots = 2 * grid
-  int nqb;
-  int Lq;
-  int heads;
-  int out_f32;
-  int nsplit;
-  int item[kMaxSplit];
-  int first[kMaxSplit + 1];  // parts of split k: slot[first[k] .. first[k+1])
-  int slot[2 * kMaxSplit];
+  Sched s;
+  float* part;  // scratch: partial O [2*grid][NQ*BM][D], then m and l [2*grid][NQ*BM] each
 };
 
 // ----------------------------------------------------------------------------
-// PTX wrappers
+// PTX wrappers of the one-CTA kernel
 // ----------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ uint64_t now_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
-struct Ctl {
-  volatile int* abort;
-  unsigned* err;
-  long long timeout_ns;
-};
-
-__device__ __noinline__ bool wait_slow(uint32_t bar, uint32_t parity, const Ctl& c) {
-  const uint64_t t0 = now_ns();
-  while (true) {
-    if (mbar_try(bar, parity)) return true;
-    if (*c.abort) return false;
-    if ((long long)(now_ns() - t0) > c.timeout_ns) {
-      *c.abort = 1;
-      *reinterpret_cast<volatile unsigned*>(c.err) = kErrTimeout;
-      __threadfence_system();
-      return false;
-    }
-  }
-}
-// Bounded wait for the phase of `bar` with the given parity; false = abort.
-__device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity, const Ctl& c) {
-  if (mbar_try(bar, parity)) return true;
-  return wait_slow(bar, parity, c);
-}
-// Bounded wait that ignores the abort flag (teardown of work in flight).
-__device__ __noinline__ void wait_drain(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = now_ns();
-  while (!mbar_try(bar, parity)) {
-    if ((long long)(now_ns() - t0) > kDrainNs) return;
-  }
-}
-
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
                                             int c2) {
   asm volatile(
@@ -182,8 +97,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 // commit from one elected lane of a converged warp
 __device__ __forceinline__ void tc_commit_e(uint32_t bar) {
   asm volatile(
@@ -191,75 +104,6 @@ __device__ __forceinline__ void tc_commit_e(uint32_t bar) {
       "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
       : "memory");
 }
-#define LL_R8(i) "=r"(r[i + 0]), "=r"(r[i + 1]), "=r"(r[i + 2]), "=r"(r[i + 3]), \
-                 "=r"(r[i + 4]), "=r"(r[i + 5]), "=r"(r[i + 6]), "=r"(r[i + 7])
-#define LL_W8(i) "r"(r[i + 0]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), \
-                 "r"(r[i + 4]), "r"(r[i + 5]), "r"(r[i + 6]), "r"(r[i + 7])
-
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : LL_R8(0), LL_R8(8), LL_R8(16), LL_R8(24)
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : LL_R8(0), LL_R8(8)
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-          taddr),
-      LL_W8(0), LL_W8(8)
-      : "memory");
-}
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-// Orders later uses of loaded registers after tcgen05.wait::ld.
-__device__ __forceinline__ void reg_fence(uint32_t* r, int n) {
-#pragma unroll
-  for (int i = 0; i < n; ++i) asm volatile("" : "+r"(r[i]));
-}
-
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-// max of three floats in one instruction
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-  float d;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-  return d;
-}
-__device__ __forceinline__ uint64_t pack_f32x2(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-// (d0, d1) = (a0, a1) * b + c, two lanes per instruction
-__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, uint64_t b, uint64_t c) {
-  asm("{\n\t.reg .b64 a, d;\n\tmov.b64 a, {%2, %3};\n\tfma.rn.f32x2 d, a, %4, %5;\n\tmov.b64 {%0, %1}, d;\n\t}"
-      : "=f"(d0), "=f"(d1)
-      : "f"(a0), "f"(a1), "l"(b), "l"(c));
-}
-// s0 += low bf16 of pk, s1 += high bf16 of pk (widened exactly, fp32 adds)
-__device__ __forceinline__ void add_bf16x2(float& s0, float& s1, uint32_t pk) {
-  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tadd.rn.f32.bf16 %0, lo, %0;\n\t"
-      "add.rn.f32.bf16 %1, hi, %1;\n\t}"
-      : "+f"(s0), "+f"(s1)
-      : "r"(pk));
-}
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  uint32_t r;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-  return r;
-}
-
 // Eight (or four) MMAs of one group from a single asm block, issued by the lane
 // that elect.sync picks (the whole warp executes the block; operands are the
 // same in every lane): k-step 0 accumulates when acc != 0, the others always.
@@ -300,131 +144,6 @@ __device__ __forceinline__ void mma4_ts(uint32_t d, uint32_t a, const uint64_t (
       "add.u32 t, %2, 16;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], %5, %1, p1;\n\t"
       "add.u32 t, %2, 24;\n\t@e tcgen05.mma.cta_group::1.kind::f16 [%0], [t], %6, %1, p1;\n\t}" ::"r"(d),
       "r"(idesc), "r"(a), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc));
-}
-
-// Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
-// address, leading and stride byte offsets in 16-byte units, version 1).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-__device__ __forceinline__ uint64_t make_desc(uint32_t lo, uint32_t hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
-  return r;
-}
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M x N, A/B major-ness.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-// ----------------------------------------------------------------------------
-// Work schedule
-// ----------------------------------------------------------------------------
-// Attend mode: an item is (head, 256-row query block); every item has the same
-// nkv key tiles.  The grid is persistent (at most one CTA per SM).  Whole
-// rounds of items come first -- CTA c takes item r*grid + c in round r, so the
-// CTAs sweep the K/V tiles of a few heads in step and each tile is fetched
-// from HBM about once -- and the items left over (fewer than the grid) are cut
-// into equal runs of key tiles across `tail_ctas` CTAs.  A run that covers only
-// part of an item leaves a partial result (unnormalised O, reference max m and
-// sum l per row) in scratch slot 2*c + (0: first run of CTA c, 1: its last
-// run); combine_kernel merges the parts of each split item.  Mode 2 (masked
-// attend) uses the same schedule.
-// Prefill mode (mode 1): items are numbered from the last query block to the
-// first, i.e. longest first (block g of a block-causal prefill sees g + 1
-// blocks of keys); round r gives CTA c item r*grid + c (r even) or
-// r*grid + grid - 1 - c (r odd), which keeps every CTA's total within one item
-// of the mean without splitting any item.
-struct Piece {
-  int item;
-  int j0, j1;   // key tiles [j0, j1) of the item
-  int partial;  // 1: write a partial result to scratch slot `slot`
-  int slot;
-};
-
-struct Walker {
-  int r;
-  long long it, end, begin;
-  int prefill;
-};
-
-__host__ __device__ __forceinline__ void walker_init(Walker& w, const TcParams& p, int cta) {
-  w.r = 0;
-  w.prefill = p.a.mode == 1;
-  w.begin = w.end = 0;
-  if (!w.prefill && cta < p.tail_ctas) {
-    w.begin = (p.tail_iters * cta) / p.tail_ctas;
-    w.end = (p.tail_iters * (cta + 1)) / p.tail_ctas;
-  }
-  w.it = w.begin;
-}
-
-// Key tiles a prefill item of query block qb needs: every cached tile (source A,
-// fully visible) and the fresh tiles up to the end of the block of its last row.
-__host__ __device__ __forceinline__ int prefill_nkv(const TcParams& p, int qb) {
-  const AttendArgs& a = p.a;
-  const int qend = (qb + 1) * NQ * BM;
-  const int qlast = (qend < a.Lq ? qend : a.Lq) - 1;
-  const long long e = ((long long)qlast / a.block_tokens + 1) * a.block_tokens;
-  const int kv_end = (int)(e < a.Lb ? e : a.Lb);
-  return (a.La + BN - 1) / BN + (kv_end + BN - 1) / BN;
-}
-
-__host__ __device__ __forceinline__ bool walker_next(Walker& w, const TcParams& p, Piece& pc, int cta) {
-  if (w.prefill) {
-    // items come longest first; round r hands them out left to right (even r) or
-    // right to left (odd r), so each CTA's total stays close to the mean
-    const int items = p.nqb * p.a.heads;
-    while (w.r * p.grid < items) {
-      const int r = w.r++;
-      const int item = r * p.grid + ((r & 1) ? p.grid - 1 - cta : cta);
-      if (item >= items) continue;
-      pc.item = item;
-      pc.j0 = 0;
-      pc.j1 = prefill_nkv(p, p.nqb - 1 - item / p.a.heads);
-      pc.partial = 0;
-      pc.slot = 0;
-      return true;
-    }
-    return false;
-  }
-  if (w.r < p.rounds) {
-    pc.item = w.r * p.grid + cta;
-    pc.j0 = 0;
-    pc.j1 = p.nkv;
-    pc.partial = 0;
-    pc.slot = 0;
-    ++w.r;
-    return true;
-  }
-  if (w.it >= w.end) return false;
-  const long long ti = w.it / p.nkv;
-  const int j0 = (int)(w.it - ti * p.nkv);
-  const long long stop = w.end - ti * p.nkv;
-  const int j1 = (int)(stop < p.nkv ? stop : p.nkv);
-  pc.item = p.rounds * p.grid + (int)ti;
-  pc.j0 = j0;
-  pc.j1 = j1;
-  pc.partial = !(j0 == 0 && j1 == p.nkv);
-  pc.slot = 2 * cta + (w.it == w.begin ? 0 : 1);
-  w.it = ti * p.nkv + j1;
-  return true;
-}
-
-// head, first query row and cache-tile count of an item
-__device__ __forceinline__ void item_geom(const TcParams& p, int item, int& head, int& q0, int& nA) {
-  if (p.a.mode != 1) {
-    head = item / p.nqb;
-    q0 = (item - head * p.nqb) * NQ * BM;
-    nA = (p.a.La + BN - 1) / BN;
-  } else {
-    const int qb = p.nqb - 1 - item / p.a.heads;
-    head = item - (item / p.a.heads) * p.a.heads;
-    q0 = qb * NQ * BM;
-    nA = (p.a.La + BN - 1) / BN;
-  }
 }
 
 // ----------------------------------------------------------------------------
@@ -495,13 +214,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       // ------------------------------ TMA producer ------------------------------
       asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&p.tm_q)) : "memory");
       Walker wk;
-      walker_init(wk, p, blockIdx.x);
+      walker_init(wk, p.a, p.s, blockIdx.x);
       Piece pc;
       int u = 0;
       bool ok = true;
-      while (ok && walker_next(wk, p, pc, blockIdx.x)) {
+      while (ok && walker_next(wk, p.a, p.s, pc, blockIdx.x)) {
         int head, q0, nA;
-        item_geom(p, pc.item, head, q0, nA);
+        item_geom(p.a, p.s, pc.item, head, q0, nA);
         // the previous item's Q K^T products must be done with the Q tiles
         if (q_issued > 0 && !(ok = wait(bQempty, (q_issued - 1) & 1, ctl))) break;
         mbar_expect_tx(bQfull, NQ * Cf::kQBytes);
@@ -579,11 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         mma4_ts(tmem + 128 * w, tmem + 256 + 128 * w + 32 * half, bd, kIdPV, acc ? 1u : 0u);
       };
       Walker wk;
-      walker_init(wk, p, blockIdx.x);
+      walker_init(wk, p.a, p.s, blockIdx.x);
       Piece pc;
       int u = 0, qi = 0, jt = 0;
       bool ok = true;
-      while (ok && walker_next(wk, p, pc, blockIdx.x)) {
+      while (ok && walker_next(wk, p.a, p.s, pc, blockIdx.x)) {
         const int n = pc.j1 - pc.j0;
         if (!(ok = __all_sync(0xffffffffu, wait(bQfull, qi & 1, ctl)))) break;
         if (!(ok = __all_sync(0xffffffffu, wait(bKVfull0 + 8 * (u % NS), (u / NS) & 1, ctl)))) break;
@@ -647,13 +366,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     const uint32_t bP2 = bP0 + 16 + 8 * w;  // P of keys 64-127 stored
     const float sl2 = a.scale_log2;
     Walker wk;
-    walker_init(wk, p, blockIdx.x);
+    walker_init(wk, p.a, p.s, blockIdx.x);
     Piece pc;
     int qi = 0, jt = 0;
     bool ok = true;
-    while (ok && walker_next(wk, p, pc, blockIdx.x)) {
+    while (ok && walker_next(wk, p.a, p.s, pc, blockIdx.x)) {
       int head, q0, nA;
-      item_geom(p, pc.item, head, q0, nA);
+      item_geom(p.a, p.s, pc.item, head, q0, nA);
       const int qrow = q0 + w * BM + row;
       int row_end = a.Lb;
       if (a.mode != 0) {
@@ -753,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       tc_fence_after();
       if (pc.partial) {
         // unnormalised O with its reference max and sum, merged by combine_kernel
-        const size_t rows_all = (size_t)2 * p.grid * (NQ * BM);
+        const size_t rows_all = (size_t)2 * p.s.grid * (NQ * BM);
         const size_t sr = (size_t)pc.slot * (NQ * BM) + w * BM + row;
         float* po = p.part + sr * D;
 #pragma unroll 1
@@ -809,6 +528,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
   }
 
   // ------------------------------ teardown ------------------------------------
+  // this CTA's work is issued: the launch that follows (merge of split items or
+  // the commit copy) may be scheduled; it waits for this grid to complete
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __syncthreads();
   if (warp == 0 && lane == 0) {
     // copies still in flight land before the shared memory is released
@@ -832,219 +554,82 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
   }
 }
 
-// ----------------------------------------------------------------------------
-// Merge of split items: out = sum_p 2^(m_p - M) O_p / sum_p 2^(m_p - M) l_p
-// ----------------------------------------------------------------------------
-template <int D>
-__global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ CombineParams c) {
-  constexpr int E = D / 32;
-  const int k = blockIdx.x;
-  const int r = blockIdx.y * 8 + (threadIdx.x >> 5);  // row within the item's 256 query rows
-  const int lane = threadIdx.x & 31;
-  const int item = c.item[k];
-  const int head = item / c.nqb;
-  const int qrow = (item - head * c.nqb) * NQ * BM + r;
-  if (qrow >= c.Lq) return;
-  const size_t rows_all = (size_t)2 * c.grid * (NQ * BM);
-  const float* pm = c.part + rows_all * D;
-  const float* pl = pm + rows_all;
-  float M = -INFINITY;
-  for (int i = c.first[k]; i < c.first[k + 1]; ++i) M = fmaxf(M, pm[(size_t)c.slot[i] * (NQ * BM) + r]);
-  float acc[E], L = 0.f;
-#pragma unroll
-  for (int e = 0; e < E; ++e) acc[e] = 0.f;
-  for (int i = c.first[k]; i < c.first[k + 1]; ++i) {
-    const size_t sr = (size_t)c.slot[i] * (NQ * BM) + r;
-    const float mi = pm[sr];
-    const float wgt = (mi == -INFINITY) ? 0.f : exp2f(mi - M);
-    L += wgt * pl[sr];
-    const float* o = c.part + sr * D + lane * E;
-#pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = fmaf(wgt, o[e], acc[e]);
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
-  const int64_t ob = ((int64_t)qrow * c.heads + head) * D + lane * E;
-  if (c.out_f32) {
-    float* out = static_cast<float*>(c.out) + ob;
-#pragma unroll
-    for (int e = 0; e < E; ++e) out[e] = acc[e] * inv;
-  } else {
-    __nv_bfloat16* out = static_cast<__nv_bfloat16*>(c.out) + ob;
-#pragma unroll
-    for (int e = 0; e < E; ++e) out[e] = __float2bfloat16_rn(acc[e] * inv);
-  }
-}
-
-// ----------------------------------------------------------------------------
-// Host side: tensor maps, schedule and launch
-// ----------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
-  return fn;
-}
-
-bool encode3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1, uint64_t s2,
-              uint32_t b0, uint32_t b1, uint32_t b2) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {d0, d1, d2};
-  cuuint64_t strides[2] = {s1, s2};
-  cuuint32_t box[3] = {b0, b1, b2};
-  cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// [L][H][D] token tensor, boxes of 64 d x 1 head x 128 tokens.
-bool encode_tokens(CUtensorMap* m, const void* base, int L, int H, int D) {
-  return encode3d(m, base, (uint64_t)D, (uint64_t)H, (uint64_t)L, (uint64_t)D * 2, (uint64_t)H * D * 2, 64, 1, 128);
-}
-
-int sm_count() {
-  int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-  return n;
-}
-
-constexpr int kMinTailTiles = 16;  // shortest run of key tiles a tail CTA takes
-
-// Schedule of an attend launch (see "Work schedule"); fills p and the split list.
-void plan_attend(TcParams& p, CombineParams& cp, int max_ctas) {
-  const AttendArgs& a = p.a;
-  const int items = p.nqb * a.heads;
-  p.nkv = (a.La + BN - 1) / BN + (a.Lb + BN - 1) / BN;
-  int g = max_ctas < kMaxSplit ? max_ctas : kMaxSplit;
-  if (g > items) g = items;
-  if (g < 1) g = 1;
-  p.grid = g;
-  p.rounds = items / g;
-  const int rem = items - p.rounds * g;
-  p.tail_iters = (long long)rem * p.nkv;
-  long long tc = p.tail_iters / kMinTailTiles;
-  if (tc > g) tc = g;
-  if (tc < 1) tc = 1;
-  p.tail_ctas = rem > 0 ? (int)tc : 0;
-  cp.nsplit = 0;
-  int np = 0;
-  auto bnd = [&](long long cta) { return (p.tail_iters * cta) / p.tail_ctas; };
-  int c = 0;
-  for (int ti = 0; ti < rem; ++ti) {
-    const long long lo = (long long)ti * p.nkv, hi = lo + p.nkv;
-    while (c + 1 < p.tail_ctas && bnd(c + 1) <= lo) ++c;
-    int chi = c;
-    while (chi + 1 < p.tail_ctas && bnd(chi + 1) < hi) ++chi;
-    if (chi == c) continue;
-    const int k = cp.nsplit++;
-    cp.item[k] = p.rounds * p.grid + ti;
-    cp.first[k] = np;
-    cp.slot[np++] = 2 * c + (bnd(c) == lo ? 0 : 1);
-    for (int cc = c + 1; cc <= chi; ++cc) cp.slot[np++] = 2 * cc;
-  }
-  cp.first[cp.nsplit] = np;
-}
-
 template <int D>
 cudaError_t launch_tc(const AttendArgs& a, cudaStream_t stream) {
   TcParams p;
   std::memset(&p, 0, sizeof(p));
   p.a = a;
-  const int La = a.La > 0 ? a.La : 1;
-  if (!encode_tokens(&p.tm_q, a.q, a.Lq, a.heads, D) || !encode_tokens(&p.tm_kn, a.kn, a.Lb, a.heads, D) ||
-      !encode_tokens(&p.tm_vn, a.vn, a.Lb, a.heads, D) ||
-      !encode3d(&p.tm_kc, a.kc, D, (uint64_t)La, (uint64_t)a.heads, (uint64_t)D * 2,
-                (uint64_t)a.cache_head_elems * 2, 64, 128, 1) ||
-      !encode3d(&p.tm_vc, a.vc, D, (uint64_t)La, (uint64_t)a.heads, (uint64_t)D * 2,
-                (uint64_t)a.cache_head_elems * 2, 64, 128, 1))
+  if (!encode_tokens(&p.tm_q, a.q, a.Lq, a.heads, D, BM) || !encode_tokens(&p.tm_kn, a.kn, a.Lb, a.heads, D, BN) ||
+      !encode_tokens(&p.tm_vn, a.vn, a.Lb, a.heads, D, BN) ||
+      !encode_cache(&p.tm_kc, a.kc, a.La, a.heads, D, a.cache_head_elems, BN) ||
+      !encode_cache(&p.tm_vc, a.vc, a.La, a.heads, D, a.cache_head_elems, BN))
     return cudaErrorInvalidValue;
-  p.nqb = (a.Lq + NQ * BM - 1) / (NQ * BM);
+  p.s.nqb = (a.Lq + NQ * BM - 1) / (NQ * BM);
   CombineParams cp;
   cp.nsplit = 0;
   if (a.mode == 1) {
     // persistent: one CTA per SM, items in zigzag rounds (see walker_next)
-    const int items = p.nqb * a.heads;
+    const int items = p.s.nqb * a.heads;
     const int sms = sm_count();
-    p.grid = items < sms ? items : sms;
+    p.s.grid = items < sms ? items : sms;
   } else {
     // without scratch for two partial results per CTA, no item is split
     int ctas = sm_count();
     if (2 * ctas > a.scratch_slots) ctas = a.scratch_slots / 2;
-    plan_attend(p, cp, ctas < 1 ? 1 : ctas);
+    plan_attend(a, p.s, cp, ctas < 1 ? 1 : ctas);
     if (cp.nsplit > 0 && !a.scratch) return cudaErrorInvalidValue;
     p.part = a.scratch;
   }
-  static int attr_done[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64 || !attr_done[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(attend_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         Cfg<D>::kSmemBytes);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64) attr_done[dev] = 1;
-  }
-  attend_tc_kernel<D><<<(unsigned)p.grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(p);
+  static std::atomic<int> attr_done[64];
+  if (cudaError_t e = smem_opt_in(attend_tc_kernel<D>, Cfg<D>::kSmemBytes, attr_done)) return e;
+  attend_tc_kernel<D><<<(unsigned)p.s.grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(p);
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || cp.nsplit == 0) return e;
-  cp.out = a.out;
-  cp.part = p.part;
-  cp.grid = p.grid;
-  cp.nqb = p.nqb;
-  cp.Lq = a.Lq;
-  cp.heads = a.heads;
-  cp.out_f32 = a.out_f32;
-  combine_kernel<D><<<dim3((unsigned)cp.nsplit, (NQ * BM) / 8), 256, 0, stream>>>(cp);
-  count_launch();
-  return cudaGetLastError();
+  return launch_combine<D>(cp, a, p.s, p.part, stream);
 }
 
 }  // namespace
 
 size_t attend_scratch_bytes(int head_dim, int slots) {
-  return (size_t)slots * (NQ * BM) * (head_dim + 2) * sizeof(float);
+  return (size_t)slots * tc::kItemRows * (head_dim + 2) * sizeof(float);
 }
 
 int attend_scratch_slots_wanted() {
-  int n = sm_count();
-  if (n > kMaxSplit) n = kMaxSplit;
+  int n = tc::sm_count();
+  if (n > tc::kMaxSplit) n = tc::kMaxSplit;
   return 2 * n;
 }
 
 int attend_schedule_dump(int Lq, int La, int Lb, int heads, int max_ctas, int mode, int block_tokens, int* grid,
                          int* out, int cap, int* splits, int split_cap, int* split_ints) {
-  TcParams p;
-  std::memset(&p, 0, sizeof(p));
-  p.a.Lq = Lq;
-  p.a.La = La;
-  p.a.Lb = Lb;
-  p.a.heads = heads;
-  p.a.mode = mode;
-  p.a.block_tokens = block_tokens;
-  p.nqb = (Lq + NQ * BM - 1) / (NQ * BM);
+  using namespace tc;
+  AttendArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.Lq = Lq;
+  a.La = La;
+  a.Lb = Lb;
+  a.heads = heads;
+  a.mode = mode;
+  a.block_tokens = block_tokens;
+  Sched sc;
+  std::memset(&sc, 0, sizeof(sc));
+  sc.nqb = (Lq + kItemRows - 1) / kItemRows;
   CombineParams cp;
   cp.nsplit = 0;
   if (mode == 1) {
-    const int items = p.nqb * heads;
-    p.grid = items < max_ctas ? items : max_ctas;
+    const int items = sc.nqb * heads;
+    sc.grid = items < max_ctas ? items : max_ctas;
   } else {
-    plan_attend(p, cp, max_ctas);
+    plan_attend(a, sc, cp, max_ctas);
   }
-  *grid = p.grid;
+  *grid = sc.grid;
   int n = 0;
-  for (int c = 0; c < p.grid; ++c) {
+  for (int c = 0; c < sc.grid; ++c) {
     Walker wk;
-    walker_init(wk, p, c);
+    walker_init(wk, a, sc, c);
     Piece pc;
-    while (walker_next(wk, p, pc, c)) {
+    while (walker_next(wk, a, sc, pc, c)) {
       if (n + 6 <= cap) {
         out[n + 0] = c;
         out[n + 1] = pc.item;
@@ -1072,7 +657,8 @@ int attend_schedule_dump(int Lq, int La, int Lb, int heads, int max_ctas, int mo
 }
 
 cudaError_t launch_attend_bf16_tc(const AttendArgs& a, cudaStream_t stream) {
-  return a.head_dim == 64 ? launch_tc<64>(a, stream) : launch_tc<128>(a, stream);
+  if (a.head_dim == 64) return launch_tc<64>(a, stream);
+  return a.pair ? launch_attend_bf16_pair(a, stream) : launch_tc<128>(a, stream);
 }
 
 }  // namespace ll

@@ -12,6 +12,12 @@
 // of the cache and reads two whole 256-byte rows of the source (bf16, d = 128).
 // A block's slab is one (frame, head) pair: a frame's T tokens of one head are
 // contiguous in the cache.
+//
+// The copy is launched as a programmatic dependent of the kernel before it on the
+// stream (the attention launch of the same call, for a commit): its blocks may be
+// scheduled while that kernel drains, and each one waits (griddepcontrol.wait)
+// until the predecessor has completed and its memory is visible before it reads
+// or writes anything, so the launch latency is hidden and the order is kept.
 #include "ll_internal.h"
 
 namespace ll {
@@ -24,6 +30,7 @@ constexpr int kUnroll = 4;  // 16-byte vectors per thread per tensor
 // grid.y = source frame * heads + head; grid.x covers that (frame, head) slab of
 // T rows x vpr vectors.  All index math stays in 32 bits within one slab.
 __global__ void __launch_bounds__(kThreads) copy_frames_kernel(const __grid_constant__ CopyFramesArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int f = blockIdx.y / a.heads;
   const int h = blockIdx.y - f * a.heads;
   const int slot = a.slot_of[f];
@@ -66,11 +73,11 @@ cudaError_t launch_copy_frames(const CopyFramesArgs& a, cudaStream_t stream) {
   if (a.frames <= 0) return cudaSuccess;
   const int vpr = a.head_dim * a.elem_bytes / 16;
   const int slab = a.tokens_per_frame * vpr;
-  dim3 grid((unsigned)((slab + kThreads * kUnroll - 1) / (kThreads * kUnroll)),
-            (unsigned)(a.frames * a.heads));
-  copy_frames_kernel<<<grid, kThreads, 0, stream>>>(a);
+  const dim3 grid((unsigned)((slab + kThreads * kUnroll - 1) / (kThreads * kUnroll)),
+                  (unsigned)(a.frames * a.heads));
+  const cudaError_t e = launch_dependent(copy_frames_kernel, grid, dim3(kThreads), 0, stream, a);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace ll

@@ -44,6 +44,7 @@ struct ll_cache {
   int stall_inject = 0;
   int stall_timeout_us = 0;
   int use_simt = 0;
+  int pair = 0;           // head_dim 128 on the CTA-pair tensor-core kernel (test hook)
   int out_f32 = 0;        // outputs in fp32 on a bf16 cache
   int chunk_mask = LL_MASK_CHUNK;
   int recache_scope = LL_RECACHE_RESIDENT;
@@ -122,6 +123,7 @@ ll::AttendArgs base_args(ll_cache* c, int layer) {
   a.out_f32 = (c->dtype == LL_FP32 || c->out_f32) ? 1 : 0;
   a.scratch = c->scratch;
   a.scratch_slots = c->scratch_slots;
+  a.pair = c->pair;
   a.stall_inject = c->stall_inject;
   a.timeout_ns = c->stall_inject ? (long long)c->stall_timeout_us * 1000LL : kDefaultTimeoutNs;
   c->stall_inject = 0;  // one launch only
@@ -565,6 +567,12 @@ int ll_debug_attend_schedule(int Lq, int La, int Lb, int heads, int max_ctas, in
 ll_status ll_debug_use_simt(ll_cache* c, int enable) {
   if (!c) return LL_ERR_INVALID_ARG;
   c->use_simt = enable ? 1 : 0;
+  return LL_OK;
+}
+
+ll_status ll_debug_pair_kernel(ll_cache* c, int enable) {
+  if (!c) return LL_ERR_INVALID_ARG;
+  c->pair = enable ? 1 : 0;
   return LL_OK;
 }
 

@@ -67,9 +67,13 @@ struct AttendArgs {
   long long timeout_ns;
   float* scratch;     // partial results of split work items (tensor-core kernel)
   int scratch_slots;  // partial-result slots the scratch holds
+  int pair;           // head_dim 128: the CTA-pair tensor-core kernel instead of the one-CTA kernel
 };
 
+// bf16 attention on the tensor cores: the one-CTA kernel, or for head_dim 128 with
+// a.pair the CTA-pair kernel.
 cudaError_t launch_attend_bf16_tc(const AttendArgs& a, cudaStream_t stream);
+cudaError_t launch_attend_bf16_pair(const AttendArgs& a, cudaStream_t stream);
 // Scratch of the tensor-core kernel: bytes for `slots` partial results, and the
 // slot count it uses on the current device (two per SM).
 size_t attend_scratch_bytes(int head_dim, int slots);
@@ -82,5 +86,25 @@ int attend_schedule_dump(int Lq, int La, int Lb, int heads, int max_ctas, int mo
 cudaError_t launch_attend_simt(const AttendArgs& a, int elem_bytes, cudaStream_t stream);
 
 void count_launch();
+
+// Launch `kernel` as a programmatic dependent of the kernel before it on `stream`
+// (programmatic stream serialization): its blocks may be scheduled while that
+// kernel drains.  The kernel must execute griddepcontrol.wait before its first
+// access to memory that earlier work on the stream writes or reads.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                    cudaStream_t stream, const Args&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
 
 }  // namespace ll
