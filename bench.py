@@ -374,20 +374,36 @@ def timed_region(args, world, local, caches, step, profile_every=1):
 
 
 def attend_kernel_name(args):
+    if args.key_fp8:
+        return "attend_tc_kernel<128, e4m3 keys>"
     return "attend_pair_kernel (CTA pair)" if args.pair else "attend_tc_kernel<128>"
 
 
-def tensor_roofline(kernel, flops, n, ms, pk, pk_src, sustained=True):
-    """Tensor-bound roofline object of one kernel: flops over its summed CUDA-event time."""
+def cache_dtype(ll, args):
+    return ll.LL_BF16_K8 if args.key_fp8 else ll.LL_BF16
+
+
+def peak_scale(args):
+    """Tensor peak of the attention relative to the bf16 peak.  With e4m3 keys Q K^T (half
+    the flops) runs at the FP8 rate, twice the bf16 rate (the nominal ratio, 4.5 / 2.25
+    PFLOP/s), and P V at the bf16 rate: 1 / (0.5 / 2 + 0.5 / 1) = 4 / 3."""
+    return 4.0 / 3.0 if args.key_fp8 else 1.0
+
+
+def tensor_roofline(kernel, flops, n, ms, pk, pk_src, sustained=True, scale=1.0):
+    """Tensor-bound roofline object of one kernel: flops over its summed CUDA-event time.
+    scale: the kernel's peak relative to the bf16 peak (4/3 with e4m3 keys, see peak_scale)."""
     achieved = flops / (ms / 1e3) / 1e12 if ms > 0 else 0.0
     key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
-    peak = pk.get(key, FALLBACK[key])
+    peak = pk.get(key, FALLBACK[key]) * scale
+    src = "%s %s (%s)" % (pk_src, key, "kernel timed inside a long step" if sustained else "kernel timed in isolation")
+    if scale != 1.0:
+        src += " x %.4g: Q K^T at the FP8 rate (2x bf16, nominal ratio), P V at the bf16 rate" % scale
     return {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak,
-            "peak_source": "%s %s (%s)" % (pk_src, key, "kernel timed inside a long step" if sustained
-                                           else "kernel timed in isolation"),
-            "frac_of_burst_peak": achieved / pk.get("bf16_tflops", FALLBACK["bf16_tflops"]),
-            "frac_of_nominal_2250": achieved / 2250.0,
+            "peak_source": src,
+            "frac_of_burst_peak": achieved / (pk.get("bf16_tflops", FALLBACK["bf16_tflops"]) * scale),
+            "frac_of_nominal_2250": achieved / (2250.0 * scale),
             "launches": n, "ms_per_launch": ms / max(n, 1), "flops_per_launch": flops / max(n, 1)}
 
 
@@ -403,7 +419,7 @@ def base_result(args, world, value, ms_max, config):
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (keys e4m3)" if args.key_fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) q/k/v per layer and chunk, Wan2.1-1.3B shapes; no weights)",
         "config": config,
     }
@@ -433,7 +449,7 @@ def run_ours(args, world, rank, local):
     inputs = [[tuple(llsynth.seeded_normal(("bench", rank, l, c, t), (L, H, d), device="cuda") for t in "qkv")
                for c in range(chunks)] for l in range(shape.layers)]
     outs = [torch.empty((L, H, d), dtype=torch.bfloat16, device="cuda") for _ in range(shape.layers)]
-    cache = ll.ll_cache_create(shape.layers, H, d, T, S, W, C, ll.LL_BF16)
+    cache = ll.ll_cache_create(shape.layers, H, d, T, S, W, C, cache_dtype(ll, args))
     set_options(ll, cache, args)
     stream = torch.cuda.current_stream()
 
@@ -464,11 +480,11 @@ def run_ours(args, world, rank, local):
         "chunk_mask": args.chunk_mask, "recache_scope": args.recache_scope,
         "parallelism": "replicas x%d (independent streams, no collective)" % world}))
     result = base_result(args, world, step_frames * args.steps * world / (ms_max / 1e3), ms_max, config)
-    roof = tensor_roofline(attend_kernel_name(args), att_sampled, n_att, ms_att, pk, pk_src)
+    roof = tensor_roofline(attend_kernel_name(args), att_sampled, n_att, ms_att, pk, pk_src, scale=peak_scale(args))
     roof["sampling"] = "one launch in ten of each kind bracketed with CUDA events in the timed region"
     alg = sum(attend_bytes(shape, resident_count(S, W, t0)) for t0, _ in plan) / len(plan)
     roof["algorithmic_bytes_per_launch"] = alg
-    roof["traffic"], src = traffic_per_launch(alg) if not args.pair else (None, None)
+    roof["traffic"], src = traffic_per_launch(alg) if not (args.pair or args.key_fp8) else (None, None)
     if src:
         roof["traffic_source"] = "ncu capture of %s, scaled by algorithmic bytes" % src
     in_stream = hbm_roofline("copy_frames_kernel", cp_sampled, n_cp, ms_cp, pk)
@@ -476,7 +492,7 @@ def run_ours(args, world, rank, local):
     result.update({
         "tflops": step_flops * args.steps * world / (ms_max / 1e3) / 1e12,
         "roofline": roof,
-        "append": append_batch(ll, cache, shape, inputs, pk),
+        "append": append_batch(ll, cache, shape, inputs, pk) if not args.key_fp8 else None,
         "append_in_stream_brackets": in_stream,
         "gpu_launches": launches,
         "clocks": clocks,
@@ -585,7 +601,7 @@ def run_single(args, world, rank, local):
                         shape.window_frames, shape.chunk_frames)
     L = C * T
     passes = llsynth.SINGLE_LAYER_PASSES
-    cache = ll.ll_cache_create(1, H, d, T, S, W, C, ll.LL_BF16)
+    cache = ll.ll_cache_create(1, H, d, T, S, W, C, cache_dtype(ll, args))
     set_options(ll, cache, args)
     for c in range((S + W) // C):
         q, k, v = (llsynth.seeded_normal(("bench-single-fill", rank, c, t), (L, H, d), device="cuda",
@@ -616,10 +632,10 @@ def run_single(args, world, rank, local):
                                        "chunk_mask": args.chunk_mask}))
     result = base_result(args, world, C * args.steps * world / (ms_max / 1e3), ms_max, config)
     roof = tensor_roofline(attend_kernel_name(args), pass_flops * passes * args.steps, n_att, ms_att, pk, pk_src,
-                           sustained=False)
+                           sustained=False, scale=peak_scale(args))
     alg = attend_bytes(shape, S + W)
     roof["algorithmic_bytes_per_launch"] = alg
-    roof["traffic"], src = traffic_per_launch(alg) if not args.pair else (None, None)
+    roof["traffic"], src = traffic_per_launch(alg) if not (args.pair or args.key_fp8) else (None, None)
     if src:
         roof["traffic_source"] = "ncu capture of %s" % src
     result.update({
@@ -651,7 +667,7 @@ def run_recache30(args, world, rank, local):
                  for l in range(shape.layers)]
     outs = [torch.empty((L, H, d), dtype=torch.bfloat16, device="cuda") for _ in range(shape.layers)]
     out_rc = torch.empty((R * T, H, d), dtype=torch.bfloat16, device="cuda")
-    cache = ll.ll_cache_create(shape.layers, H, d, T, S, W, C, ll.LL_BF16)
+    cache = ll.ll_cache_create(shape.layers, H, d, T, S, W, C, cache_dtype(ll, args))
     set_options(ll, cache, args)
     stream = torch.cuda.current_stream()
     plan = stream_plan(shape, chunks)
@@ -685,9 +701,10 @@ def run_recache30(args, world, rank, local):
     result = base_result(args, world, chunks * C * args.steps * world / (ms_max / 1e3), ms_max, config)
     result.update({
         "tflops": (att_flops + step_pre_flops) * args.steps * world / (ms_max / 1e3) / 1e12,
-        "roofline": tensor_roofline(attend_kernel_name(args), att_flops * args.steps, n_att, ms_att, pk, pk_src),
+        "roofline": tensor_roofline(attend_kernel_name(args), att_flops * args.steps, n_att, ms_att, pk, pk_src,
+                                    scale=peak_scale(args)),
         "prefill": dict(tensor_roofline(attend_kernel_name(args) + " (prefill mode)", step_pre_flops * args.steps, n_pre,
-                                        ms_pre, pk, pk_src),
+                                        ms_pre, pk, pk_src, scale=peak_scale(args)),
                         ms_per_switch_30_layers=ms_pre / max(1, args.steps * switches)),
         "gpu_launches": launches, "clocks": clocks,
     })
@@ -710,7 +727,7 @@ def run_sweep(args, world, rank, local):
     rows, total_ms, total_frames = [], 0.0, 0
     for W in llsynth.SWEEP_W:
         for S in llsynth.SWEEP_S:
-            cache = ll.ll_cache_create(1, H, d, T, S, W, C, ll.LL_BF16)
+            cache = ll.ll_cache_create(1, H, d, T, S, W, C, cache_dtype(ll, args))
             set_options(ll, cache, args)
             while ll.ll_cache_state(cache, 0)[0] < S + W + C:  # steady state: sink and window full
                 ll.ll_attend_chunk(cache, 0, *inputs[0], out, True)
@@ -863,6 +880,8 @@ def main():
                     help="chunk (default): a chunk sees all its frames; frame: the frame-causal reading")
     ap.add_argument("--recache-scope", choices=["resident", "window"], default="resident",
                     help="resident (default): recache rewrites sink and window; window: the sink keeps its K/V")
+    ap.add_argument("--key-fp8", action="store_true",
+                    help="an FP8-key cache (LL_BF16_K8): keys stored in e4m3, Q K^T at the FP8 tensor rate")
     ap.add_argument("--pair", action="store_true",
                     help="run head_dim 128 on the CTA-pair tensor-core kernel instead of the default one-CTA kernel")
     ap.add_argument("--ref-budget-s", type=float, default=None,

@@ -52,8 +52,19 @@ extern "C" {
 
 typedef struct ll_cache ll_cache; /* opaque */
 
-/* Element type of the cache and of every token tensor. */
-typedef enum { LL_BF16 = 0, LL_FP32 = 1 } ll_dtype;
+/*
+ * Element type of the cache and of every token tensor.
+ *   LL_BF16, LL_FP32: tokens and both caches in that type.
+ *   LL_BF16_K8: token tensors (q, k, v, out, windows) and the V cache in bf16;
+ *     the K cache holds every key rounded to FP8 e4m3 (one byte: round to
+ *     nearest even, saturating at +-448), and Q K^T runs on the FP8 tensor-core
+ *     path (tcgen05.mma kind::f8f6f4) with q and the fresh keys rounded the same
+ *     way; P V, the softmax statistics and out are as in LL_BF16.  The K cache
+ *     takes half the bytes.  head_dim 128 only.  (The pages report INT8
+ *     inference (Abstract, §5 Conclusion); rounding the keys is a defined input
+ *     step, so results match attention over the rounded q and k.)
+ */
+typedef enum { LL_BF16 = 0, LL_FP32 = 1, LL_BF16_K8 = 2 } ll_dtype;
 
 typedef enum {
   LL_OK = 0,
@@ -72,10 +83,12 @@ LL_API const char* ll_status_str(ll_status s);
  * ll_cache_create -- allocate the per-layer KV caches.
  * §3.3 "Short window attention": the cache is sized by the window, not by the
  * video length: K and V each hold layers * H * (S + W) * T * d elements,
- * head-major [layer][head][slot][token][d].  The memory is cudaMalloc'ed on
- * the current device and zero-filled; ll_cache_destroy frees it.
+ * head-major [layer][head][slot][token][d] (K one byte per element with
+ * LL_BF16_K8).  The memory is cudaMalloc'ed on the current device and
+ * zero-filled; ll_cache_destroy frees it.
  * Requirements: layers, heads, tokens_per_frame, chunk_frames >= 1;
- * sink_frames, window_frames >= 0; head_dim in {64, 128}.  Limits of the
+ * sink_frames, window_frames >= 0; head_dim in {64, 128} (128 for
+ * LL_BF16_K8).  Limits of the
  * library, beyond which the call returns LL_ERR_UNSUPPORTED: S + W <= 512 and
  * C <= 512 frames, heads <= 127 (the commit copy runs 512 x heads blocks at
  * most), (S + W + C) * T <= 2^30 tokens.  Returns LL_ERR_OOM if the
@@ -188,14 +201,16 @@ LL_API ll_status ll_cache_state(ll_cache* cache, int layer, int64_t* frames_comm
 /*
  * ll_cache_read -- copy one layer's raw cache to HOST buffers, each
  * H * (S + W) * T * d elements in the head-major slot layout (for tests;
- * synchronises the device).
+ * synchronises the device).  With LL_BF16_K8 host_k receives the e4m3 bytes
+ * (one per element) and host_v bf16.
  */
 LL_API ll_status ll_cache_read(ll_cache* cache, int layer, void* host_k, void* host_v);
 
 /* Wait for all work on the device; report a pending device error, if any. */
 LL_API ll_status ll_sync(ll_cache* cache);
 
-/* Sizes of a cache: S + W slots, bytes of one layer's K (same for V), element size. */
+/* Sizes of a cache: S + W slots, bytes of one layer's K cache and the size of a K element
+ * (V: the same, except LL_BF16_K8, whose V elements take 2 bytes and K elements 1). */
 LL_API ll_status ll_cache_info(const ll_cache* cache, int* slots, size_t* layer_bytes, int* elem_bytes);
 
 /*
@@ -243,7 +258,8 @@ LL_API ll_status ll_debug_inject_stall(ll_cache* cache, int enable, int timeout_
 /*
  * Test hook: a non-zero value routes this cache's bf16 attention through the
  * CUDA-core kernel that serves the fp32 dtype (one warp per query row) instead
- * of the tensor-core kernel, so tests can compare the two CUDA kernels.
+ * of the tensor-core kernel, so tests can compare the two CUDA kernels.  An
+ * LL_BF16_K8 cache ignores it (its keys need the FP8 tensor-core path).
  */
 LL_API ll_status ll_debug_use_simt(ll_cache* cache, int enable);
 
@@ -252,7 +268,7 @@ LL_API ll_status ll_debug_use_simt(ll_cache* cache, int enable);
  * through the CTA-pair tensor-core kernel (two SMs share every MMA, M = 256;
  * slower than the default one-CTA kernel on B300) instead of the one-CTA
  * kernel, so tests and benchmarks can run both on the same inputs.  Other
- * head dims ignore it.
+ * head dims and LL_BF16_K8 caches ignore it.
  */
 LL_API ll_status ll_debug_pair_kernel(ll_cache* cache, int enable);
 

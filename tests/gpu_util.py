@@ -76,7 +76,16 @@ def sample_rows(L: int, n: int, seed: int = 0) -> np.ndarray:
 
 
 def bits(t: torch.Tensor) -> torch.Tensor:
+    if t.element_size() == 1:
+        return t.view(torch.uint8)
     return t.view(torch.int16) if t.element_size() == 2 else t.view(torch.int32)
+
+
+def round_e4m3(t: torch.Tensor) -> torch.Tensor:
+    """bf16 values rounded to FP8 e4m3 as the library rounds keys and queries for an
+    LL_BF16_K8 cache: nearest value, ties to even, saturating at +-448 (torch's own
+    conversion returns NaN past 480, hence the clamp).  Returns a float8_e4m3fn CPU tensor."""
+    return torch.clamp(t.detach().cpu().float(), -448.0, 448.0).to(torch.float8_e4m3fn)
 
 
 class Lockstep:
@@ -86,9 +95,12 @@ class Lockstep:
     (CPU tensors), so the raw cache bytes can be compared slot by slot.
     """
 
-    def __init__(self, ll, layers, heads, head_dim, T, S, W, C, dtype, keep_frames=True):
+    def __init__(self, ll, layers, heads, head_dim, T, S, W, C, dtype, keep_frames=True, key_fp8=False):
+        """key_fp8: an LL_BF16_K8 cache (bf16 tokens, e4m3 key cache); the oracle is fed q and k
+        rounded to e4m3 as the library rounds them, and the raw K slots hold e4m3 bytes."""
         self.ll = ll
-        self.cache = ll.ll_cache_create(layers, heads, head_dim, T, S, W, C, dtype)
+        self.key_fp8 = key_fp8
+        self.cache = ll.ll_cache_create(layers, heads, head_dim, T, S, W, C, ll.LL_BF16_K8 if key_fp8 else dtype)
         self.orc = oracle.OracleCache(layers, heads, head_dim, T, S, W, C)
         self.shape = (layers, heads, head_dim, T, S, W, C)
         self.dtype = dtype
@@ -105,21 +117,29 @@ class Lockstep:
     def C(self):
         return self.shape[6]
 
+    def qk64(self, t):
+        """q or k as the oracle sees them: rounded to e4m3 first for an FP8-key cache."""
+        return f64(round_e4m3(t)) if self.key_fp8 else f64(t)
+
+    def key_store(self, k):
+        """What the K cache stores for keys k (CPU): the e4m3 bytes for an FP8-key cache."""
+        return round_e4m3(k).view(torch.uint8) if self.key_fp8 else k.cpu()
+
     def attend(self, layer, q, k, v, commit, rows=None, check=True, what=""):
         """q, k, v: CUDA tensors.  Returns the GPU output (and checks it unless check=False)."""
         out = torch.empty(q.shape, dtype=self.cache.out_dtype, device=q.device)
         self.ll.ll_attend_chunk(self.cache, layer, q, k, v, out, commit)
         if check:
-            qh, kh, vh = f64(q), f64(k), f64(v)
+            qh, kh, vh = self.qk64(q), self.qk64(k), f64(v)
             want = self.orc.attend(layer, qh, kh, vh, commit, rows=rows)
             got = out if rows is None else out[torch.as_tensor(rows, device=out.device)]
             compare(got, want, what or "attend", atol=self.atol)
         elif commit:
-            kh, vh = f64(k), f64(v)
+            kh, vh = self.qk64(k), f64(v)
             self.orc.commit(layer, kh, vh)
         if commit and self.keep:
             t0 = self.orc.state(layer)[0] - self.C
-            kc, vc = k.cpu(), v.cpu()
+            kc, vc = self.key_store(k), v.cpu()
             for i in range(self.C):
                 self.host[layer][t0 + i] = (kc[i * self.T:(i + 1) * self.T], vc[i * self.T:(i + 1) * self.T])
         return out
@@ -146,25 +166,25 @@ class Lockstep:
 
     def recache(self, layer, k_win, v_win):
         self.ll.ll_recache(self.cache, layer, k_win, v_win)
-        self.orc.recache(layer, f64(k_win), f64(v_win))
+        self.orc.recache(layer, self.qk64(k_win), f64(v_win))
         self._keep_recache(layer, k_win, v_win)
 
     def recache_attend(self, layer, q_win, k_win, v_win, rows=None, check=True, what=""):
         out = torch.empty(q_win.shape, dtype=self.cache.out_dtype, device=q_win.device)
         self.ll.ll_recache_attend(self.cache, layer, q_win, k_win, v_win, out)
         if check:
-            want = self.orc.recache_attend(layer, f64(q_win), f64(k_win), f64(v_win), rows=rows)
+            want = self.orc.recache_attend(layer, self.qk64(q_win), self.qk64(k_win), f64(v_win), rows=rows)
             got = out if rows is None else out[torch.as_tensor(rows, device=out.device)]
             compare(got, want, what or "recache prefill", atol=self.atol)
         else:
-            self.orc.recache(layer, f64(k_win), f64(v_win))
+            self.orc.recache(layer, self.qk64(k_win), f64(v_win))
         self._keep_recache(layer, k_win, v_win)
         return out
 
     def _keep_recache(self, layer, k_win, v_win):
         if not self.keep:
             return
-        kc, vc = k_win.cpu(), v_win.cpu()
+        kc, vc = self.key_store(k_win), v_win.cpu()
         for i, f in enumerate(self.orc.recache_frames(layer)):
             self.host[layer][f] = (kc[i * self.T:(i + 1) * self.T], vc[i * self.T:(i + 1) * self.T])
 

@@ -166,3 +166,29 @@ def test_noalloc_rejects_an_output_that_overlaps_an_input(ll):
         assert call(out) == ll.LL_ERR_UNSUPPORTED, hex(out - base)
     # with no cached rows the cached pointers are ignored
     assert call(kc, cached_tokens=0) == ll.LL_ERR_UNSUPPORTED
+
+
+def test_e4m3_rounding_helper_matches_the_format_definition():
+    """The tests' e4m3 rounding (torch conversion after a clamp to +-448) against rounding
+    written from the format: 3 mantissa bits, exponent bias 7 (normals down to 2^-6, then
+    subnormals spaced 2^-9), nearest value with ties to even, saturating at +-448."""
+    import numpy as np
+    import torch
+
+    from tests.gpu_util import round_e4m3
+
+    def e4m3_from_definition(x):
+        ax = np.abs(x)
+        e = np.maximum(np.floor(np.log2(np.maximum(ax, 2.0 ** -30))), -6)
+        step = 2.0 ** (e - 3)
+        return np.sign(x) * np.minimum(np.round(ax / step) * step, 448.0)
+
+    rng = np.random.default_rng(0)
+    vals = [rng.standard_normal(20000) * s for s in (0.003, 0.05, 1, 8, 100)]
+    ties = [(8 + m) * 2.0 ** (e - 3) + 2.0 ** (e - 4) for e in range(-6, 9) for m in range(8)]
+    ties += [m * 2.0 ** -9 + 2.0 ** -10 for m in range(8)]
+    vals += [np.array(ties), -np.array(ties), np.array([447.9, 448.0, 460.0, 470.0, 1000.0, -1000.0, 0.0])]
+    x = torch.from_numpy(np.concatenate(vals)).to(torch.bfloat16)
+    got = round_e4m3(x).double().numpy()
+    want = e4m3_from_definition(x.double().numpy())
+    assert np.array_equal(got, want)

@@ -68,11 +68,18 @@ constexpr int NS = 5;          // stages of the K/V tile ring
 constexpr int kThreads = 384;
 static_assert(NQ * BM == kItemRows, "a CTA takes one work item");
 
-template <int D>
+// K8: Q and K in e4m3 (one byte per element; Q K^T on kind::f8f6f4), V in bf16.
+template <int D, bool K8>
 struct Cfg {
-  static constexpr int kChunks = D / 64;              // 64-element (128-byte) column chunks
-  static constexpr int kTileBytes = BN * D * 2;       // one K or V tile
-  static constexpr int kQBytes = BM * D * 2;          // one Q tile
+  static constexpr int kQKElem = K8 ? 1 : 2;                // bytes per Q / K element
+  static constexpr int kQKChunks = D * kQKElem / 128;       // 128-byte column chunks of Q and K
+  static constexpr int kQKBox = 128 / kQKElem;              // elements per such chunk
+  static constexpr int kVChunks = D / 64;                   // 128-byte column chunks of V (bf16)
+  static constexpr int kKSteps = D * kQKElem / 32;          // 32-byte k-steps of one Q K^T product
+  static constexpr int kKBytes = BN * D * kQKElem;          // one K tile
+  static constexpr int kVBytes = BN * D * 2;                // one V tile
+  static constexpr int kTileBytes = kVBytes;                // one ring stage (K or V)
+  static constexpr int kQBytes = BM * D * kQKElem;          // one Q tile
   static constexpr int kSmemKV = NQ * kQBytes;
   static constexpr int kSmemBar = kSmemKV + NS * kTileBytes;
   static constexpr int kSmemBytes = kSmemBar + 256 + 1024;  // barriers, then alignment slack
@@ -123,6 +130,17 @@ __device__ __forceinline__ void mma8_ss(uint32_t d, const uint64_t (&a)[8], cons
       "r"(idesc), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]),
       "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(acc));
 }
+// Four k-steps of kind::f8f6f4 (e4m3 A and B, 32 elements per k-step), S = Q K^T.
+__device__ __forceinline__ void mma4_ss_f8(uint32_t d, const uint64_t (&a)[4], const uint64_t (&b)[4],
+                                           uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p0, 0, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %2, %6, %1, p0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %3, %7, %1, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %4, %8, %1, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %5, %9, %1, p1;\n\t}" ::"r"(d),
+      "r"(idesc), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]));
+}
 __device__ __forceinline__ void mma4_ss(uint32_t d, const uint64_t (&a)[4], const uint64_t (&b)[4], uint32_t idesc,
                                         uint32_t acc) {
   asm volatile(
@@ -149,9 +167,9 @@ __device__ __forceinline__ void mma4_ts(uint32_t d, uint32_t a, const uint64_t (
 // ----------------------------------------------------------------------------
 // The kernel
 // ----------------------------------------------------------------------------
-template <int D>
+template <int D, bool K8>
 __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_constant__ TcParams p) {
-  using Cf = Cfg<D>;
+  using Cf = Cfg<D, K8>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -225,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         if (q_issued > 0 && !(ok = wait(bQempty, (q_issued - 1) & 1, ctl))) break;
         mbar_expect_tx(bQfull, NQ * Cf::kQBytes);
         for (int w = 0; w < NQ; ++w)
-          for (int c = 0; c < Cf::kChunks; ++c)
-            tma_load_3d(sQ + (w * Cf::kChunks + c) * kAtom, &p.tm_q, bQfull, c * 64, head, q0 + w * BM);
+          for (int c = 0; c < Cf::kQKChunks; ++c)
+            tma_load_3d(sQ + w * Cf::kQBytes + c * kAtom, &p.tm_q, bQfull, c * Cf::kQKBox, head, q0 + w * BM);
         ++q_issued;
         for (int j = pc.j0; ok && j < pc.j1; ++j) {
           for (int is_v = 0; is_v < 2; ++is_v) {
@@ -234,15 +252,16 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
             const int use = u / NS;
             if (use > 0 && !(ok = wait(bKVempty0 + 8 * s, (use - 1) & 1, ctl))) break;
             const uint32_t full = bKVfull0 + 8 * s;
-            mbar_expect_tx(full, Cf::kTileBytes);
+            mbar_expect_tx(full, is_v ? Cf::kVBytes : Cf::kKBytes);
             const uint32_t dst = sKV + s * Cf::kTileBytes;
+            const int nc = is_v ? Cf::kVChunks : Cf::kQKChunks;
+            const int cw = is_v ? 64 : Cf::kQKBox;  // elements per 128-byte chunk
             if (j < nA) {
               const CUtensorMap* m = is_v ? &p.tm_vc : &p.tm_kc;
-              for (int c = 0; c < Cf::kChunks; ++c) tma_load_3d(dst + c * kAtom, m, full, c * 64, j * BN, head);
+              for (int c = 0; c < nc; ++c) tma_load_3d(dst + c * kAtom, m, full, c * cw, j * BN, head);
             } else {
               const CUtensorMap* m = is_v ? &p.tm_vn : &p.tm_kn;
-              for (int c = 0; c < Cf::kChunks; ++c)
-                tma_load_3d(dst + c * kAtom, m, full, c * 64, head, (j - nA) * BN);
+              for (int c = 0; c < nc; ++c) tma_load_3d(dst + c * kAtom, m, full, c * cw, head, (j - nA) * BN);
             }
             tiles_issued = ++u;
           }
@@ -252,7 +271,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
   } else if (warp == 1) {
     {
       // ------------------------------ MMA issuer (whole warp) --------------------
-      constexpr uint32_t kIdQK = idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
+      constexpr uint32_t kIdQK = K8 ? idesc_e4m3(BM, BN) : idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
       constexpr uint32_t kIdPV = idesc_bf16(BM, D, 0, 1);   // P from TMEM; V is N(=d)-major
       // The tensor core takes one 128x128x16 MMA per 64 clocks, but this warp
       // shares its SMSP's issue slots with two busy softmax warps and gets few of
@@ -267,13 +286,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       // tile differ from the ring's first stage only in the start address field
       // of the low word (16-byte units; shared offsets stay below 256 KB, so no
       // carry reaches the high word).
-      static_assert(D / 16 == 8 || D / 16 == 4, "k-steps per Q K^T group");
+      constexpr int KS = Cf::kKSteps;
+      static_assert(KS == 8 || KS == 4, "k-steps per Q K^T group");
       static_assert(BN / 16 == 8, "k-steps per P V group");
-      uint64_t dq[NQ][D / 16];
+      uint64_t dq[NQ][KS];
 #pragma unroll
       for (int w = 0; w < NQ; ++w)
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
+        for (int ks = 0; ks < KS; ++ks)
           dq[w][ks] = sw128_desc(sQ + w * Cf::kQBytes + (ks >> 2) * kAtom + (ks & 3) * 32, 16, 1024);
       const uint64_t dK0 = sw128_desc(sKV, 16, 1024);
       const uint64_t dV0 = sw128_desc(sKV, kAtom, 1024);
@@ -281,10 +301,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       const uint32_t v_lo0 = (uint32_t)dV0, v_hi = (uint32_t)(dV0 >> 32);
       auto issue_qk = [&](int w, int stage) {
         const uint32_t lo = k_lo0 + (((uint32_t)stage * Cf::kTileBytes) >> 4);
-        uint64_t bd[D / 16];
+        uint64_t bd[KS];
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) bd[ks] = make_desc(lo + ((ks >> 2) * kAtom + (ks & 3) * 32) / 16, k_hi);
-        if constexpr (D / 16 == 8)
+        for (int ks = 0; ks < KS; ++ks) bd[ks] = make_desc(lo + ((ks >> 2) * kAtom + (ks & 3) * 32) / 16, k_hi);
+        if constexpr (K8)
+          mma4_ss_f8(tmem + 256 + 128 * w, dq[w], bd, kIdQK);
+        else if constexpr (KS == 8)
           mma8_ss(tmem + 256 + 128 * w, dq[w], bd, kIdQK, 0u);
         else
           mma4_ss(tmem + 256 + 128 * w, dq[w], bd, kIdQK, 0u);
@@ -554,14 +576,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
   }
 }
 
-template <int D>
+template <int D, bool K8>
 cudaError_t launch_tc(const AttendArgs& a, cudaStream_t stream) {
+  constexpr int qk = K8 ? 1 : 2;  // bytes per Q / K element
   TcParams p;
   std::memset(&p, 0, sizeof(p));
   p.a = a;
-  if (!encode_tokens(&p.tm_q, a.q, a.Lq, a.heads, D, BM) || !encode_tokens(&p.tm_kn, a.kn, a.Lb, a.heads, D, BN) ||
-      !encode_tokens(&p.tm_vn, a.vn, a.Lb, a.heads, D, BN) ||
-      !encode_cache(&p.tm_kc, a.kc, a.La, a.heads, D, a.cache_head_elems, BN) ||
+  if (!encode_tokens(&p.tm_q, a.q, a.Lq, a.heads, D, BM, qk) ||
+      !encode_tokens(&p.tm_kn, a.kn, a.Lb, a.heads, D, BN, qk) || !encode_tokens(&p.tm_vn, a.vn, a.Lb, a.heads, D, BN) ||
+      !encode_cache(&p.tm_kc, a.kc, a.La, a.heads, D, a.cache_head_elems, BN, qk) ||
       !encode_cache(&p.tm_vc, a.vc, a.La, a.heads, D, a.cache_head_elems, BN))
     return cudaErrorInvalidValue;
   p.s.nqb = (a.Lq + NQ * BM - 1) / (NQ * BM);
@@ -581,8 +604,8 @@ cudaError_t launch_tc(const AttendArgs& a, cudaStream_t stream) {
     p.part = a.scratch;
   }
   static std::atomic<int> attr_done[64];
-  if (cudaError_t e = smem_opt_in(attend_tc_kernel<D>, Cfg<D>::kSmemBytes, attr_done)) return e;
-  attend_tc_kernel<D><<<(unsigned)p.s.grid, kThreads, Cfg<D>::kSmemBytes, stream>>>(p);
+  if (cudaError_t e = smem_opt_in(attend_tc_kernel<D, K8>, Cfg<D, K8>::kSmemBytes, attr_done)) return e;
+  attend_tc_kernel<D, K8><<<(unsigned)p.s.grid, kThreads, Cfg<D, K8>::kSmemBytes, stream>>>(p);
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || cp.nsplit == 0) return e;
@@ -657,8 +680,9 @@ int attend_schedule_dump(int Lq, int La, int Lb, int heads, int max_ctas, int mo
 }
 
 cudaError_t launch_attend_bf16_tc(const AttendArgs& a, cudaStream_t stream) {
-  if (a.head_dim == 64) return launch_tc<64>(a, stream);
-  return a.pair ? launch_attend_bf16_pair(a, stream) : launch_tc<128>(a, stream);
+  if (a.qk_fp8) return a.head_dim == 128 ? launch_tc<128, true>(a, stream) : cudaErrorInvalidValue;
+  if (a.head_dim == 64) return launch_tc<64, false>(a, stream);
+  return a.pair ? launch_attend_bf16_pair(a, stream) : launch_tc<128, false>(a, stream);
 }
 
 }  // namespace ll

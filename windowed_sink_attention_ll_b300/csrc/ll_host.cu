@@ -30,11 +30,14 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 struct ll_cache {
   int L, H, D, T, S, W, C;
   ll_dtype dtype;
-  int eb;                 // element bytes
+  int eb;                 // element bytes of the token tensors and of the V cache
+  int keb;                // element bytes of the K cache (1: e4m3 keys, LL_BF16_K8)
   int device;
   size_t layer_elems;     // elements of one layer's K (= V)
   void* k = nullptr;      // [L][H][S+W][T][D]
   void* v = nullptr;
+  uint8_t* q8 = nullptr;  // LL_BF16_K8: q and the chunk's (or recache window's) keys rounded to e4m3
+  uint8_t* k8 = nullptr;
   std::vector<int64_t> n;               // frames committed per layer
   std::vector<int64_t> fos;             // frame_of_slot, L x (S+W)
   unsigned* err_host = nullptr;         // mapped host word written by kernels
@@ -112,10 +115,11 @@ ll_status set_device(const ll_cache* c) {
 ll::AttendArgs base_args(ll_cache* c, int layer) {
   ll::AttendArgs a;
   std::memset(&a, 0, sizeof(a));
-  const size_t off = c->layer_elems * (size_t)layer * (size_t)c->eb;
-  a.kc = static_cast<const char*>(c->k) + off;
-  a.vc = static_cast<const char*>(c->v) + off;
+  const size_t off = c->layer_elems * (size_t)layer;
+  a.kc = static_cast<const char*>(c->k) + off * c->keb;
+  a.vc = static_cast<const char*>(c->v) + off * c->eb;
   a.cache_head_elems = (int64_t)(c->S + c->W) * c->T * c->D;
+  a.qk_fp8 = c->dtype == LL_BF16_K8 ? 1 : 0;
   a.heads = c->H;
   a.head_dim = c->D;
   a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)c->D));
@@ -165,7 +169,16 @@ struct ProfileScope {
 ll_status launch_attend(ll_cache* c, const ll::AttendArgs& a, cudaStream_t st, int kind) {
   ProfileScope prof(c, st, kind);
   cudaError_t e;
-  if (c->dtype == LL_FP32 || c->use_simt) {
+  if (c->dtype == LL_BF16_K8) {
+    // keys in e4m3: the attention reads q and its fresh keys rounded the same way,
+    // from the cache's staging buffers (which a commit copy then reads); every
+    // caller here has as many fresh keys as queries
+    ll::AttendArgs a8 = a;
+    e = ll::launch_quantize_e4m3(a.q, c->q8, a.kn, c->k8, (int64_t)a.Lq * c->H * c->D, st);
+    a8.q = c->q8;
+    a8.kn = c->k8;
+    if (e == cudaSuccess) e = ll::launch_attend_bf16_tc(a8, st);
+  } else if (c->dtype == LL_FP32 || c->use_simt) {
     e = ll::launch_attend_simt(a, c->eb, st);
   } else {
     e = ll::launch_attend_bf16_tc(a, st);
@@ -178,11 +191,12 @@ ll_status launch_copy(ll_cache* c, int layer, const void* k, const void* v, cons
                       cudaStream_t st) {
   ll::CopyFramesArgs a;
   std::memset(&a, 0, sizeof(a));
-  const size_t off = c->layer_elems * (size_t)layer * (size_t)c->eb;
+  const size_t off = c->layer_elems * (size_t)layer;
   a.src_k = k;
   a.src_v = v;
-  a.dst_k = static_cast<char*>(c->k) + off;
-  a.dst_v = static_cast<char*>(c->v) + off;
+  a.dst_k = static_cast<char*>(c->k) + off * c->keb;
+  a.dst_v = static_cast<char*>(c->v) + off * c->eb;
+  a.k_elem_bytes = c->keb;
   a.frames = (int)slot_of.size();
   a.tokens_per_frame = c->T;
   a.heads = c->H;
@@ -245,8 +259,9 @@ ll_status ll_cache_create(ll_cache** out, int layers, int heads, int head_dim, i
   if (layers < 1 || heads < 1 || tokens_per_frame < 1 || chunk_frames < 1 || sink_frames < 0 ||
       window_frames < 0)
     return LL_ERR_INVALID_ARG;
-  if (dtype != LL_BF16 && dtype != LL_FP32) return LL_ERR_INVALID_ARG;
+  if (dtype != LL_BF16 && dtype != LL_FP32 && dtype != LL_BF16_K8) return LL_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return LL_ERR_UNSUPPORTED;
+  if (dtype == LL_BF16_K8 && head_dim != 128) return LL_ERR_UNSUPPORTED;
   const int slots = sink_frames + window_frames;
   if (slots > ll::kMaxFrameTable || chunk_frames > ll::kMaxFrameTable) return LL_ERR_UNSUPPORTED;
   // kernel grids: (frames x heads) copy blocks; 32-bit token counts per call
@@ -262,7 +277,8 @@ ll_status ll_cache_create(ll_cache** out, int layers, int heads, int head_dim, i
   c->W = window_frames;
   c->C = chunk_frames;
   c->dtype = dtype;
-  c->eb = dtype == LL_BF16 ? 2 : 4;
+  c->eb = dtype == LL_FP32 ? 4 : 2;
+  c->keb = dtype == LL_BF16_K8 ? 1 : c->eb;
   c->layer_elems = (size_t)heads * slots * tokens_per_frame * head_dim;
   c->n.assign(layers, 0);
   c->fos.assign((size_t)layers * slots, -1);
@@ -272,49 +288,40 @@ ll_status ll_cache_create(ll_cache** out, int layers, int heads, int head_dim, i
   }
   // at least one 256-byte block, so a cache without slots (S = W = 0) still
   // hands the kernels a valid base address
-  size_t bytes = c->layer_elems * layers * c->eb;
-  if (bytes < 256) bytes = 256;
-  {
-    if (cudaMalloc(&c->k, bytes) != cudaSuccess) {
-      cudaGetLastError();
-      delete c;
-      return LL_ERR_OOM;
-    }
-    if (cudaMalloc(&c->v, bytes) != cudaSuccess) {
-      cudaGetLastError();
-      cudaFree(c->k);
-      delete c;
-      return LL_ERR_OOM;
-    }
-    if (cudaMemset(c->k, 0, bytes) != cudaSuccess || cudaMemset(c->v, 0, bytes) != cudaSuccess) {
-      cudaFree(c->k);
-      cudaFree(c->v);
-      delete c;
-      return LL_ERR_CUDA;
-    }
-  }
-  if (dtype == LL_BF16) {
+  size_t kbytes = c->layer_elems * layers * c->keb, vbytes = c->layer_elems * layers * c->eb;
+  if (kbytes < 256) kbytes = 256;
+  if (vbytes < 256) vbytes = 256;
+  auto fail = [&](ll_status st) {
+    cudaGetLastError();
+    cudaFree(c->k);
+    cudaFree(c->v);
+    cudaFree(c->scratch);
+    cudaFree(c->q8);
+    delete c;
+    return st;
+  };
+  if (cudaMalloc(&c->k, kbytes) != cudaSuccess || cudaMalloc(&c->v, vbytes) != cudaSuccess) return fail(LL_ERR_OOM);
+  if (cudaMemset(c->k, 0, kbytes) != cudaSuccess || cudaMemset(c->v, 0, vbytes) != cudaSuccess)
+    return fail(LL_ERR_CUDA);
+  if (dtype != LL_FP32) {
     // the tensor-core kernel splits left-over work items across SMs and merges
     // their partial results: two slots per SM
     c->scratch_slots = ll::attend_scratch_slots_wanted();
     if (cudaMalloc(reinterpret_cast<void**>(&c->scratch), ll::attend_scratch_bytes(head_dim, c->scratch_slots)) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      cudaFree(c->k);
-      cudaFree(c->v);
-      delete c;
-      return LL_ERR_OOM;
-    }
+        cudaSuccess)
+      return fail(LL_ERR_OOM);
+  }
+  if (dtype == LL_BF16_K8) {
+    // staging for q and the fresh keys rounded to e4m3: a chunk, or a recache window
+    const int frames = chunk_frames > slots ? chunk_frames : slots;
+    const size_t n = (size_t)frames * tokens_per_frame * heads * head_dim;
+    if (cudaMalloc(reinterpret_cast<void**>(&c->q8), 2 * n) != cudaSuccess) return fail(LL_ERR_OOM);
+    c->k8 = c->q8 + n;
   }
   if (cudaHostAlloc(reinterpret_cast<void**>(&c->err_host), 256, cudaHostAllocMapped) != cudaSuccess ||
       cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->err_dev), c->err_host, 0) != cudaSuccess) {
-    cudaGetLastError();
     if (c->err_host) cudaFreeHost(c->err_host);
-    cudaFree(c->k);
-    cudaFree(c->v);
-    cudaFree(c->scratch);
-    delete c;
-    return LL_ERR_CUDA;
+    return fail(LL_ERR_CUDA);
   }
   *c->err_host = 0;
   *out = c;
@@ -333,6 +340,7 @@ void ll_cache_destroy(ll_cache* c) {
   cudaFree(c->k);
   cudaFree(c->v);
   cudaFree(c->scratch);
+  cudaFree(c->q8);
   cudaFreeHost(c->err_host);
   delete c;
 }
@@ -376,7 +384,8 @@ ll_status ll_attend_chunk(ll_cache* c, int layer, const void* q, const void* k, 
     const int64_t f = t0 + i;
     if (f < c->S || f >= win_lo) slot_of[i] = ll_frame_slot(c->S, c->W, f);
   }
-  if (ll_status s = launch_copy(c, layer, k, v, slot_of, st)) return s;
+  // an e4m3 key cache takes the keys the attention just rounded
+  if (ll_status s = launch_copy(c, layer, c->dtype == LL_BF16_K8 ? c->k8 : k, v, slot_of, st)) return s;
   int64_t* fos = &c->fos[(size_t)layer * (c->S + c->W)];
   for (int i = 0; i < c->C; ++i)
     if (slot_of[i] >= 0) fos[slot_of[i]] = t0 + i;
@@ -420,6 +429,13 @@ static ll_status recache_common(ll_cache* c, int layer, const void* q_win, const
   }
   std::vector<int> slot_of(R);
   for (int i = 0; i < R; ++i) slot_of[i] = ll_frame_slot(c->S, c->W, frames[i]);
+  if (c->dtype == LL_BF16_K8) {
+    // the keys go in rounded to e4m3 (the prefill above already rounded them)
+    if (!q_win && ll::launch_quantize_e4m3(k_win, c->k8, nullptr, nullptr, (int64_t)R * c->T * c->H * c->D, st) !=
+                      cudaSuccess)
+      return LL_ERR_CUDA;
+    return launch_copy(c, layer, c->k8, v_win, slot_of, st);
+  }
   return launch_copy(c, layer, k_win, v_win, slot_of, st);
 }
 
@@ -447,7 +463,7 @@ ll_status ll_set_output_dtype(ll_cache* c, ll_dtype dtype) {
   if (!c) return LL_ERR_INVALID_ARG;
   if (dtype == LL_FP32) {
     c->out_f32 = 1;
-  } else if (dtype == LL_BF16 && c->dtype == LL_BF16) {
+  } else if (dtype == LL_BF16 && (c->dtype == LL_BF16 || c->dtype == LL_BF16_K8)) {
     c->out_f32 = 0;
   } else {
     return LL_ERR_INVALID_ARG;
@@ -494,13 +510,14 @@ ll_status ll_cache_state(ll_cache* c, int layer, int64_t* frames_committed, int6
 
 ll_status ll_cache_read(ll_cache* c, int layer, void* host_k, void* host_v) {
   if (ll_status s = check_layer(c, layer)) return s;
-  const size_t bytes = c->layer_elems * c->eb;
-  if (bytes == 0) return ll_sync(c);  // no slots (S = W = 0): nothing to copy
+  const size_t kbytes = c->layer_elems * c->keb, vbytes = c->layer_elems * c->eb;
+  if (kbytes == 0) return ll_sync(c);  // no slots (S = W = 0): nothing to copy
   if (!host_k || !host_v) return LL_ERR_INVALID_ARG;
   if (ll_status s = ll_sync(c)) return s;
-  const size_t off = bytes * (size_t)layer;
-  if (cudaMemcpy(host_k, static_cast<char*>(c->k) + off, bytes, cudaMemcpyDeviceToHost) != cudaSuccess ||
-      cudaMemcpy(host_v, static_cast<char*>(c->v) + off, bytes, cudaMemcpyDeviceToHost) != cudaSuccess)
+  if (cudaMemcpy(host_k, static_cast<char*>(c->k) + kbytes * (size_t)layer, kbytes, cudaMemcpyDeviceToHost) !=
+          cudaSuccess ||
+      cudaMemcpy(host_v, static_cast<char*>(c->v) + vbytes * (size_t)layer, vbytes, cudaMemcpyDeviceToHost) !=
+          cudaSuccess)
     return LL_ERR_CUDA;
   return LL_OK;
 }
@@ -508,8 +525,8 @@ ll_status ll_cache_read(ll_cache* c, int layer, void* host_k, void* host_v) {
 ll_status ll_cache_info(const ll_cache* c, int* slots, size_t* layer_bytes, int* elem_bytes) {
   if (!c) return LL_ERR_INVALID_ARG;
   if (slots) *slots = c->S + c->W;
-  if (layer_bytes) *layer_bytes = c->layer_elems * c->eb;
-  if (elem_bytes) *elem_bytes = c->eb;
+  if (layer_bytes) *layer_bytes = c->layer_elems * c->keb;
+  if (elem_bytes) *elem_bytes = c->keb;
   return LL_OK;
 }
 

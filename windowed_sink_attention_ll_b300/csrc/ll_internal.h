@@ -26,12 +26,19 @@ struct CopyFramesArgs {
   int tokens_per_frame;
   int heads;
   int head_dim;
-  int slots;       // S + W
-  int elem_bytes;  // 2 or 4
+  int slots;         // S + W
+  int elem_bytes;    // of V (and of K unless k_elem_bytes says otherwise): 2 or 4
+  int k_elem_bytes;  // of K: 0 = elem_bytes; 1 = e4m3 keys
   int slot_of[kMaxFrameTable];
 };
 
 cudaError_t launch_copy_frames(const CopyFramesArgs& a, cudaStream_t stream);
+
+// Round `n` bf16 values of each of two tensors to e4m3 (round to nearest even,
+// saturating at +-448), as the FP8-key cache stores keys and the kind::f8f6f4
+// Q K^T product reads q and the chunk's keys.  src1/dst1 may be null.
+cudaError_t launch_quantize_e4m3(const void* src0, void* dst0, const void* src1, void* dst1, int64_t n,
+                                 cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Attention over two key/value sources:
@@ -68,6 +75,7 @@ struct AttendArgs {
   float* scratch;     // partial results of split work items (tensor-core kernel)
   int scratch_slots;  // partial-result slots the scratch holds
   int pair;           // head_dim 128: the CTA-pair tensor-core kernel instead of the one-CTA kernel
+  int qk_fp8;         // q, kn and the cache K hold e4m3 bytes (Q K^T on kind::f8f6f4); head_dim 128
 };
 
 // bf16 attention on the tensor cores: the one-CTA kernel, or for head_dim 128 with

@@ -197,6 +197,11 @@ __device__ __forceinline__ uint64_t make_desc(uint32_t lo, uint32_t hi) {
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
   return r;
 }
+// Instruction descriptor, kind::f8f6f4: e4m3 A and B (format code 0), fp32 D, M x N,
+// both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M x N, A/B major-ness.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
@@ -451,33 +456,35 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return f;
 }
 
-// bf16 3-D tensor map, 128-byte swizzle
+// 3-D tensor map of bf16 (elem_bytes 2) or byte-sized e4m3 (elem_bytes 1) elements,
+// 128-byte swizzle
 inline bool encode3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
-                     uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2) {
+                     uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2, int elem_bytes = 2) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {d0, d1, d2};
   cuuint64_t strides[2] = {s1, s2};
   cuuint32_t box[3] = {b0, b1, b2};
   cuuint32_t es[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
 }
 
-// [L][H][D] token tensor, boxes of 64 d x 1 head x `rows` tokens.
-inline bool encode_tokens(CUtensorMap* m, const void* base, int L, int H, int D, int rows) {
-  return encode3d(m, base, (uint64_t)D, (uint64_t)H, (uint64_t)L, (uint64_t)D * 2, (uint64_t)H * D * 2, 64, 1,
-                  (uint32_t)rows);
+// [L][H][D] token tensor, boxes of 128 bytes of d x 1 head x `rows` tokens.
+inline bool encode_tokens(CUtensorMap* m, const void* base, int L, int H, int D, int rows, int elem_bytes = 2) {
+  return encode3d(m, base, (uint64_t)D, (uint64_t)H, (uint64_t)L, (uint64_t)D * elem_bytes,
+                  (uint64_t)H * D * elem_bytes, 128 / elem_bytes, 1, (uint32_t)rows, elem_bytes);
 }
 
 // Head-major cache rows of one layer, [H][rows][D] with `head_elems` between heads,
-// boxes of 64 d x `rows_box` rows x 1 head.
+// boxes of 128 bytes of d x `rows_box` rows x 1 head.
 inline bool encode_cache(CUtensorMap* m, const void* base, int La, int H, int D, int64_t head_elems,
-                         int rows_box) {
+                         int rows_box, int elem_bytes = 2) {
   const int rows = La > 0 ? La : 1;
-  return encode3d(m, base, (uint64_t)D, (uint64_t)rows, (uint64_t)H, (uint64_t)D * 2, (uint64_t)head_elems * 2, 64,
-                  (uint32_t)rows_box, 1);
+  return encode3d(m, base, (uint64_t)D, (uint64_t)rows, (uint64_t)H, (uint64_t)D * elem_bytes,
+                  (uint64_t)head_elems * elem_bytes, 128 / elem_bytes, (uint32_t)rows_box, 1, elem_bytes);
 }
 
 inline int sm_count() {
