@@ -273,6 +273,29 @@ LL_API ll_status ll_debug_use_simt(ll_cache* cache, int enable);
 LL_API ll_status ll_debug_pair_kernel(ll_cache* cache, int enable);
 
 /*
+ * Test hook: a non-zero value fills every slot of this cache that holds no
+ * resident frame with all-ones bytes (NaN in bf16, fp32 and e4m3), now and after
+ * every ll_reset, so that an attention that read a slot it should not read
+ * returns NaN.  Synchronises the device.  The environment variable LL_POISON
+ * (any value but 0) turns it on for every cache at ll_cache_create.
+ */
+LL_API ll_status ll_debug_poison(ll_cache* cache, int enable);
+
+/*
+ * Fault injection on the host, process-wide: the n-th next device allocation
+ * (LL_FAULT_ALLOC: cudaMalloc / mapped host allocation in ll_cache_create) or
+ * kernel launch step (LL_FAULT_LAUNCH: the attention of a call, or its commit /
+ * recache copy) of the library fails as if the CUDA call had failed, without
+ * making it.  The call then returns LL_ERR_OOM (allocation), LL_ERR_CUDA
+ * (mapped host allocation, launch) and changes no cache state.  n = 0 disarms.
+ * The environment variable LL_FAULT="alloc:N" and/or "launch:N" (comma-separated)
+ * arms the same when the library loads.  Returns LL_ERR_INVALID_ARG for an
+ * unknown kind or n < 0.
+ */
+typedef enum { LL_FAULT_ALLOC = 1, LL_FAULT_LAUNCH = 2 } ll_fault_kind;
+LL_API ll_status ll_debug_inject_fault(int kind, int n);
+
+/*
  * Test hook (host only, no device needed): replay the work schedule of a
  * tensor-core attention launch with Lq queries, La cached and Lb fresh keys
  * per head and at most max_ctas CTAs; mode 0 = chunk attend (persistent:

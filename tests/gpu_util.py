@@ -91,6 +91,9 @@ def round_e4m3(t: torch.Tensor) -> torch.Tensor:
 class Lockstep:
     """A libll cache and an oracle cache fed the same calls; checks state after each one.
 
+    The cache's empty slots are poisoned (NaN bytes, ll_debug_poison), now and after every
+    reset: an attention that read a slot holding no resident frame would return NaN.
+
     ``host`` keeps, per layer and frame, the exact K/V values the GPU was given
     (CPU tensors), so the raw cache bytes can be compared slot by slot.
     """
@@ -101,6 +104,8 @@ class Lockstep:
         self.ll = ll
         self.key_fp8 = key_fp8
         self.cache = ll.ll_cache_create(layers, heads, head_dim, T, S, W, C, ll.LL_BF16_K8 if key_fp8 else dtype)
+        # slots without a resident frame hold NaN bytes, so a read of one would show in the outputs
+        ll.ll_debug_poison(self.cache, True)
         self.orc = oracle.OracleCache(layers, heads, head_dim, T, S, W, C)
         self.shape = (layers, heads, head_dim, T, S, W, C)
         self.dtype = dtype

@@ -192,3 +192,15 @@ def test_e4m3_rounding_helper_matches_the_format_definition():
     got = round_e4m3(x).double().numpy()
     want = e4m3_from_definition(x.double().numpy())
     assert np.array_equal(got, want)
+
+
+def test_fault_injection_arguments():
+    """ll_debug_inject_fault takes a known kind and n >= 0 (host only)."""
+    import windowed_sink_attention_ll_b300 as ll
+
+    lib = ll._lib()
+    assert lib.ll_debug_inject_fault(ll.LL_FAULT_ALLOC, 0) == ll.LL_OK
+    assert lib.ll_debug_inject_fault(ll.LL_FAULT_LAUNCH, 0) == ll.LL_OK
+    assert lib.ll_debug_inject_fault(7, 1) == ll.LL_ERR_INVALID_ARG
+    assert lib.ll_debug_inject_fault(ll.LL_FAULT_ALLOC, -1) == ll.LL_ERR_INVALID_ARG
+    assert lib.ll_debug_poison(None, 1) == ll.LL_ERR_INVALID_ARG

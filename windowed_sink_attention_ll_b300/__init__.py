@@ -37,10 +37,12 @@ EXPORTS = ("ll_status_str", "ll_cache_create", "ll_cache_destroy", "ll_attend_ch
            "ll_cache_info", "ll_frame_slot", "ll_resident_frames", "ll_launch_count",
            "ll_debug_inject_stall", "ll_debug_use_simt", "ll_profile_enable", "ll_profile_read",
            "ll_set_output_dtype", "ll_debug_attend_schedule", "ll_attend_chunk_noalloc",
-           "ll_set_chunk_mask", "ll_set_recache_scope", "ll_recache_tokens", "ll_debug_pair_kernel")
+           "ll_set_chunk_mask", "ll_set_recache_scope", "ll_recache_tokens", "ll_debug_pair_kernel",
+           "ll_debug_poison", "ll_debug_inject_fault")
 LL_KERNEL_ATTEND, LL_KERNEL_PREFILL, LL_KERNEL_COPY = 0, 1, 2
 LL_MASK_CHUNK, LL_MASK_FRAME = 0, 1
 LL_RECACHE_RESIDENT, LL_RECACHE_WINDOW = 0, 1
+LL_FAULT_ALLOC, LL_FAULT_LAUNCH = 1, 2
 
 
 class LLError(RuntimeError):
@@ -80,6 +82,8 @@ def _lib() -> ctypes.CDLL:
             "ll_debug_inject_stall": (i32, [vp, i32, i32]),
             "ll_debug_use_simt": (i32, [vp, i32]),
             "ll_debug_pair_kernel": (i32, [vp, i32]),
+            "ll_debug_poison": (i32, [vp, i32]),
+            "ll_debug_inject_fault": (i32, [i32, i32]),
             "ll_profile_enable": (i32, [vp, i32]),
             "ll_set_output_dtype": (i32, [vp, i32]),
             "ll_debug_attend_schedule": (i32, [i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32),
@@ -298,6 +302,16 @@ def ll_debug_use_simt(cache: LLCache, enable: bool) -> None:
 def ll_debug_pair_kernel(cache: LLCache, enable: bool) -> None:
     """head_dim 128 on the CTA-pair tensor-core kernel instead of the one-CTA kernel (test hook)."""
     _check(_lib().ll_debug_pair_kernel(cache.ptr, 1 if enable else 0), "ll_debug_pair_kernel")
+
+
+def ll_debug_poison(cache: LLCache, enable: bool) -> None:
+    """Fill the slots that hold no resident frame with NaN bytes, now and after every reset (test hook)."""
+    _check(_lib().ll_debug_poison(cache.ptr, 1 if enable else 0), "ll_debug_poison")
+
+
+def ll_debug_inject_fault(kind: int, n: int) -> None:
+    """Make the n-th next allocation (LL_FAULT_ALLOC) or launch step (LL_FAULT_LAUNCH) fail (0: disarm)."""
+    _check(_lib().ll_debug_inject_fault(kind, n), "ll_debug_inject_fault")
 
 
 def ll_profile_enable(cache: LLCache, enable, every: int = 1) -> None:

@@ -16,6 +16,7 @@
 #include <vector>
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "ll.h"
 #include "ll_internal.h"
@@ -51,6 +52,7 @@ struct ll_cache {
   int out_f32 = 0;        // outputs in fp32 on a bf16 cache
   int chunk_mask = LL_MASK_CHUNK;
   int recache_scope = LL_RECACHE_RESIDENT;
+  bool poison = false;    // empty slots hold all-ones bytes (NaN in every dtype): a stray read shows
   // per-kernel timing (ll_profile_enable / ll_profile_read)
   struct Mark {
     int kind;
@@ -66,6 +68,60 @@ struct ll_cache {
 namespace {
 
 constexpr long long kDefaultTimeoutNs = 2000000000LL;  // 2 s: no legal wait comes near it
+
+// An NVTX range around each entry point that works with the device (a no-op unless a
+// profiler or another NVTX tool is attached).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+};
+
+// ---------------------------------------------------------------------------
+// Fault injection on the host (ll_debug_inject_fault, or LL_FAULT=alloc:N,launch:N in
+// the environment when the library loads): the N-th next device allocation, or kernel
+// launch step, of the library reports failure as if the CUDA call had failed.  No
+// device fault is involved: the failing call is never made.
+// ---------------------------------------------------------------------------
+std::atomic<long long> g_fault_alloc{0}, g_fault_launch{0};  // countdown; 0 = off
+
+bool fault_hit(std::atomic<long long>& c) {
+  long long v = c.load();
+  while (v > 0) {
+    if (c.compare_exchange_weak(v, v - 1)) return v == 1;
+  }
+  return false;
+}
+
+struct FaultFromEnv {
+  FaultFromEnv() {
+    const char* e = std::getenv("LL_FAULT");
+    if (!e) return;
+    // comma-separated "alloc:N" / "launch:N"
+    for (const char* p = e; *p;) {
+      long long n = 0;
+      if (std::strncmp(p, "alloc:", 6) == 0 && (n = std::atoll(p + 6)) > 0) g_fault_alloc = n;
+      if (std::strncmp(p, "launch:", 7) == 0 && (n = std::atoll(p + 7)) > 0) g_fault_launch = n;
+      const char* q = std::strchr(p, ',');
+      if (!q) break;
+      p = q + 1;
+    }
+  }
+} g_fault_from_env;
+
+cudaError_t dev_alloc(void** p, size_t n) {
+  if (fault_hit(g_fault_alloc)) return cudaErrorMemoryAllocation;
+  return cudaMalloc(p, n);
+}
+cudaError_t host_alloc_mapped(void** p, size_t n) {
+  if (fault_hit(g_fault_alloc)) return cudaErrorMemoryAllocation;
+  return cudaHostAlloc(p, n, cudaHostAllocMapped);
+}
+bool launch_fault() { return fault_hit(g_fault_launch); }
+
+bool env_poison() {
+  const char* e = std::getenv("LL_POISON");
+  return e && *e && std::strcmp(e, "0") != 0;
+}
 
 int64_t resident_count(int S, int W, int64_t n) {
   const int64_t sink = n < S ? n : S;
@@ -167,6 +223,7 @@ struct ProfileScope {
 
 // kind: LL_KERNEL_ATTEND (chunk attention) or LL_KERNEL_PREFILL (recache prefill)
 ll_status launch_attend(ll_cache* c, const ll::AttendArgs& a, cudaStream_t st, int kind) {
+  if (launch_fault()) return LL_ERR_CUDA;
   ProfileScope prof(c, st, kind);
   cudaError_t e;
   if (c->dtype == LL_BF16_K8) {
@@ -204,6 +261,7 @@ ll_status launch_copy(ll_cache* c, int layer, const void* k, const void* v, cons
   a.slots = c->S + c->W;
   a.elem_bytes = c->eb;
   for (size_t i = 0; i < slot_of.size(); ++i) a.slot_of[i] = slot_of[i];
+  if (launch_fault()) return LL_ERR_CUDA;
   ProfileScope prof(c, st, LL_KERNEL_COPY);
   const cudaError_t e = ll::launch_copy_frames(a, st);
   prof.done();
@@ -214,6 +272,36 @@ ll_status check_layer(const ll_cache* c, int layer) {
   if (!c) return LL_ERR_INVALID_ARG;
   if (layer < 0 || layer >= c->L) return LL_ERR_INVALID_ARG;
   return LL_OK;
+}
+
+// All slots of every layer back to all-ones bytes (NaN in bf16, fp32 and e4m3), after
+// the device has finished with them.
+ll_status poison_slots(ll_cache* c) {
+  if (ll_status s = set_device(c)) return s;
+  const size_t kbytes = c->layer_elems * c->L * c->keb, vbytes = c->layer_elems * c->L * c->eb;
+  if (cudaDeviceSynchronize() != cudaSuccess || cudaMemset(c->k, 0xFF, kbytes) != cudaSuccess ||
+      cudaMemset(c->v, 0xFF, vbytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+    return LL_ERR_CUDA;
+  return LL_OK;
+}
+
+// Poison every slot (of every layer and head) that holds no resident frame.
+ll_status poison_resident_gaps(ll_cache* c) {
+  if (ll_status s = set_device(c)) return s;
+  if (cudaDeviceSynchronize() != cudaSuccess) return LL_ERR_CUDA;
+  const int slots = c->S + c->W;
+  const size_t rows = (size_t)c->T * c->D;  // elements of one (head, slot)
+  for (int layer = 0; layer < c->L; ++layer)
+    for (int slot = 0; slot < slots; ++slot) {
+      if (c->fos[(size_t)layer * slots + slot] >= 0) continue;
+      for (int h = 0; h < c->H; ++h) {
+        const size_t e = c->layer_elems * layer + ((size_t)h * slots + slot) * rows;
+        if (cudaMemset(static_cast<char*>(c->k) + e * c->keb, 0xFF, rows * c->keb) != cudaSuccess ||
+            cudaMemset(static_cast<char*>(c->v) + e * c->eb, 0xFF, rows * c->eb) != cudaSuccess)
+          return LL_ERR_CUDA;
+      }
+    }
+  return cudaDeviceSynchronize() == cudaSuccess ? LL_OK : LL_ERR_CUDA;
 }
 
 }  // namespace
@@ -254,6 +342,7 @@ uint64_t ll_launch_count(void) { return ll::g_launches.load(std::memory_order_re
 
 ll_status ll_cache_create(ll_cache** out, int layers, int heads, int head_dim, int tokens_per_frame,
                           int sink_frames, int window_frames, int chunk_frames, ll_dtype dtype) {
+  NvtxRange range("ll_cache_create");
   if (!out) return LL_ERR_INVALID_ARG;
   *out = nullptr;
   if (layers < 1 || heads < 1 || tokens_per_frame < 1 || chunk_frames < 1 || sink_frames < 0 ||
@@ -300,14 +389,16 @@ ll_status ll_cache_create(ll_cache** out, int layers, int heads, int head_dim, i
     delete c;
     return st;
   };
-  if (cudaMalloc(&c->k, kbytes) != cudaSuccess || cudaMalloc(&c->v, vbytes) != cudaSuccess) return fail(LL_ERR_OOM);
-  if (cudaMemset(c->k, 0, kbytes) != cudaSuccess || cudaMemset(c->v, 0, vbytes) != cudaSuccess)
+  if (dev_alloc(&c->k, kbytes) != cudaSuccess || dev_alloc(&c->v, vbytes) != cudaSuccess) return fail(LL_ERR_OOM);
+  c->poison = env_poison();
+  const int fill = c->poison ? 0xFF : 0;
+  if (cudaMemset(c->k, fill, kbytes) != cudaSuccess || cudaMemset(c->v, fill, vbytes) != cudaSuccess)
     return fail(LL_ERR_CUDA);
   if (dtype != LL_FP32) {
     // the tensor-core kernel splits left-over work items across SMs and merges
     // their partial results: two slots per SM
     c->scratch_slots = ll::attend_scratch_slots_wanted();
-    if (cudaMalloc(reinterpret_cast<void**>(&c->scratch), ll::attend_scratch_bytes(head_dim, c->scratch_slots)) !=
+    if (dev_alloc(reinterpret_cast<void**>(&c->scratch), ll::attend_scratch_bytes(head_dim, c->scratch_slots)) !=
         cudaSuccess)
       return fail(LL_ERR_OOM);
   }
@@ -315,10 +406,10 @@ ll_status ll_cache_create(ll_cache** out, int layers, int heads, int head_dim, i
     // staging for q and the fresh keys rounded to e4m3: a chunk, or a recache window
     const int frames = chunk_frames > slots ? chunk_frames : slots;
     const size_t n = (size_t)frames * tokens_per_frame * heads * head_dim;
-    if (cudaMalloc(reinterpret_cast<void**>(&c->q8), 2 * n) != cudaSuccess) return fail(LL_ERR_OOM);
+    if (dev_alloc(reinterpret_cast<void**>(&c->q8), 2 * n) != cudaSuccess) return fail(LL_ERR_OOM);
     c->k8 = c->q8 + n;
   }
-  if (cudaHostAlloc(reinterpret_cast<void**>(&c->err_host), 256, cudaHostAllocMapped) != cudaSuccess ||
+  if (host_alloc_mapped(reinterpret_cast<void**>(&c->err_host), 256) != cudaSuccess ||
       cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->err_dev), c->err_host, 0) != cudaSuccess) {
     if (c->err_host) cudaFreeHost(c->err_host);
     return fail(LL_ERR_CUDA);
@@ -329,6 +420,7 @@ ll_status ll_cache_create(ll_cache** out, int layers, int heads, int head_dim, i
 }
 
 void ll_cache_destroy(ll_cache* c) {
+  NvtxRange range("ll_cache_destroy");
   if (!c) return;
   set_device(c);
   cudaDeviceSynchronize();
@@ -347,6 +439,7 @@ void ll_cache_destroy(ll_cache* c) {
 
 ll_status ll_attend_chunk(ll_cache* c, int layer, const void* q, const void* k, const void* v, void* out,
                           int commit, void* stream) {
+  NvtxRange range("ll_attend_chunk");
   if (ll_status s = check_layer(c, layer)) return s;
   if (!q || !k || !v || !out) return LL_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return LL_ERR_INVALID_ARG;
@@ -450,11 +543,13 @@ ll_status ll_recache_tokens(const ll_cache* c, int layer, int64_t* tokens) {
 }
 
 ll_status ll_recache(ll_cache* c, int layer, const void* k_win, const void* v_win, void* stream) {
+  NvtxRange range("ll_recache");
   return recache_common(c, layer, nullptr, k_win, v_win, nullptr, stream);
 }
 
 ll_status ll_recache_attend(ll_cache* c, int layer, const void* q_win, const void* k_win, const void* v_win,
                             void* out_win, void* stream) {
+  NvtxRange range("ll_recache_attend");
   if (!q_win || !out_win) return LL_ERR_INVALID_ARG;
   return recache_common(c, layer, q_win, k_win, v_win, out_win, stream);
 }
@@ -487,10 +582,12 @@ ll_status ll_reset(ll_cache* c) {
   if (!c) return LL_ERR_INVALID_ARG;
   std::fill(c->n.begin(), c->n.end(), 0);
   std::fill(c->fos.begin(), c->fos.end(), -1);
+  if (c->poison) return poison_slots(c);
   return LL_OK;
 }
 
 ll_status ll_sync(ll_cache* c) {
+  NvtxRange range("ll_sync");
   if (!c) return LL_ERR_INVALID_ARG;
   if (ll_status s = set_device(c)) return s;
   if (cudaDeviceSynchronize() != cudaSuccess) return LL_ERR_CUDA;
@@ -509,6 +606,7 @@ ll_status ll_cache_state(ll_cache* c, int layer, int64_t* frames_committed, int6
 }
 
 ll_status ll_cache_read(ll_cache* c, int layer, void* host_k, void* host_v) {
+  NvtxRange range("ll_cache_read");
   if (ll_status s = check_layer(c, layer)) return s;
   const size_t kbytes = c->layer_elems * c->keb, vbytes = c->layer_elems * c->eb;
   if (kbytes == 0) return ll_sync(c);  // no slots (S = W = 0): nothing to copy
@@ -584,6 +682,27 @@ int ll_debug_attend_schedule(int Lq, int La, int Lb, int heads, int max_ctas, in
 ll_status ll_debug_use_simt(ll_cache* c, int enable) {
   if (!c) return LL_ERR_INVALID_ARG;
   c->use_simt = enable ? 1 : 0;
+  return LL_OK;
+}
+
+ll_status ll_debug_poison(ll_cache* c, int enable) {
+  if (!c) return LL_ERR_INVALID_ARG;
+  c->poison = enable != 0;
+  if (!c->poison) return LL_OK;
+  // every slot not holding a resident frame gets the poison now
+  if (ll_status s = poison_resident_gaps(c)) return s;
+  return LL_OK;
+}
+
+ll_status ll_debug_inject_fault(int kind, int n) {
+  if (n < 0) return LL_ERR_INVALID_ARG;
+  if (kind == LL_FAULT_ALLOC) {
+    g_fault_alloc = n;
+  } else if (kind == LL_FAULT_LAUNCH) {
+    g_fault_launch = n;
+  } else {
+    return LL_ERR_INVALID_ARG;
+  }
   return LL_OK;
 }
 
