@@ -54,7 +54,12 @@ typedef struct ll_cache ll_cache; /* opaque */
 
 /*
  * Element type of the cache and of every token tensor.
- *   LL_BF16, LL_FP32: tokens and both caches in that type.
+ *   LL_BF16, LL_FP32: tokens and both caches in that type.  At head_dim 64 an
+ *     LL_FP32 cache runs on the tensor cores with tf32 operands
+ *     (tcgen05.mma kind::tf32): Q K^T sums three tf32 products of split
+ *     operands (x = tf32(x) + tf32(x - tf32(x)), the dropped term below 2^-22
+ *     of each product), so the scores keep fp32 accuracy; P V reads P and V
+ *     rounded to tf32 (nearest).  At head_dim 128 it runs on CUDA cores in fp32.
  *   LL_BF16_K8: token tensors (q, k, v, out, windows) and the V cache in bf16;
  *     the K cache holds every key rounded to FP8 e4m3 (one byte: round to
  *     nearest even, saturating at +-448), and Q K^T runs on the FP8 tensor-core
@@ -238,7 +243,7 @@ LL_API uint64_t ll_launch_count(void);
  * merge of split work items that follows the attention kernel.
  */
 typedef enum {
-  LL_KERNEL_ATTEND = 0,  /* chunk attention (tensor-core or fp32 kernel) */
+  LL_KERNEL_ATTEND = 0,  /* chunk attention (tensor-core or CUDA-core kernel) */
   LL_KERNEL_PREFILL = 1, /* recache prefill attention */
   LL_KERNEL_COPY = 2,    /* commit / recache K,V write */
   LL_KERNEL_KINDS = 3
@@ -250,16 +255,17 @@ LL_API ll_status ll_profile_read(ll_cache* cache, int kind, int64_t* launches, d
  * Test hook: a non-zero value makes the next tensor-core attention launch of
  * this cache skip one barrier arrival so its bounded waits run out after
  * `timeout_us` microseconds; the kernel then returns early and the next call
- * reports LL_ERR_DEVICE_TIMEOUT.  0 disarms it.  The fp32 kernel has no
- * barriers and ignores it.
+ * reports LL_ERR_DEVICE_TIMEOUT.  0 disarms it.  The CUDA-core kernel (fp32
+ * at head_dim 128) has no barriers and ignores it.
  */
 LL_API ll_status ll_debug_inject_stall(ll_cache* cache, int enable, int timeout_us);
 
 /*
- * Test hook: a non-zero value routes this cache's bf16 attention through the
- * CUDA-core kernel that serves the fp32 dtype (one warp per query row) instead
- * of the tensor-core kernel, so tests can compare the two CUDA kernels.  An
- * LL_BF16_K8 cache ignores it (its keys need the FP8 tensor-core path).
+ * Test hook: a non-zero value routes this cache's bf16 or fp32 attention
+ * through the CUDA-core kernel (one warp per query row; the one fp32 at
+ * head_dim 128 runs on) instead of the tensor-core kernel, so tests can compare
+ * the two CUDA kernels.  An LL_BF16_K8 cache ignores it (its keys need the FP8
+ * tensor-core path).
  */
 LL_API ll_status ll_debug_use_simt(ll_cache* cache, int enable);
 

@@ -36,10 +36,10 @@ def ll():
     return mod
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "k8", "fp32"])
+@pytest.mark.parametrize("dtype", ["bf16", "k8", "fp32", "fp32-d64"])
 def test_allocation_failures_leave_nothing_behind(ll, dtype):
-    code = {"bf16": ll.LL_BF16, "k8": ll.LL_BF16_K8, "fp32": ll.LL_FP32}[dtype]
-    shape = (2, 4, 128, 64, 3, 6, 3)
+    code = {"bf16": ll.LL_BF16, "k8": ll.LL_BF16_K8, "fp32": ll.LL_FP32, "fp32-d64": ll.LL_FP32}[dtype]
+    shape = (2, 4, 64 if dtype == "fp32-d64" else 128, 64, 3, 6, 3)
     torch.cuda.synchronize()
     free0 = torch.cuda.mem_get_info()[0]
     failures = 0
@@ -57,8 +57,9 @@ def test_allocation_failures_leave_nothing_behind(ll, dtype):
         ll.ll_debug_inject_fault(ll.LL_FAULT_ALLOC, 0)
         cache.close()
         break
-    # bf16: K, V, split scratch, mapped error word; e4m3 keys add the rounding staging; fp32 has no scratch
-    assert failures == {"bf16": 4, "k8": 5, "fp32": 3}[dtype]
+    # bf16: K, V, split scratch, mapped error word; e4m3 keys add the rounding staging; fp32 at
+    # head_dim 128 (CUDA-core kernel) has no scratch, at head_dim 64 (tensor cores) it has
+    assert failures == {"bf16": 4, "k8": 5, "fp32": 3, "fp32-d64": 4}[dtype]
     torch.cuda.synchronize()
     assert torch.cuda.mem_get_info()[0] == free0
 

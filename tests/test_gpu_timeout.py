@@ -29,21 +29,26 @@ def ll():
     return mod
 
 
-@pytest.mark.parametrize("T,pair", [(16, False), (1040, False), (1040, True)],
-                         ids=["one-cta-small", "one-cta-persistent", "cta-pair-persistent"])
-def test_stalled_wait_times_out_and_the_cache_keeps_working(ll, T, pair):
+@pytest.mark.parametrize("T,pair,fp32", [(16, False, False), (1040, False, False), (1040, True, False),
+                                         (16, False, True), (1040, False, True)],
+                         ids=["one-cta-small", "one-cta-persistent", "cta-pair-persistent", "tf32-small",
+                              "tf32-persistent"])
+def test_stalled_wait_times_out_and_the_cache_keeps_working(ll, T, pair, fp32):
     """T = 16: one CTA per head pair; T = 1040: a persistent grid with split items, on the
     one-CTA kernel and on the CTA-pair kernel (whose two CTAs must both give up and meet
-    before they free tensor memory)."""
-    H, D, S, W, C = (2, 64, 3, 6, 3) if T == 16 else (12, 128, 3, 6, 3)
-    st = Lockstep(ll, 1, H, D, T, S, W, C, torch.bfloat16)
+    before they free tensor memory), and on the one-CTA kernel with fp32 operands (tf32,
+    head_dim 64), whose V-transpose warps wait as well."""
+    H, D, S, W, C = (2, 64, 3, 6, 3) if T == 16 else (12, 64 if fp32 else 128, 3, 6, 3)
+    dtype = torch.float32 if fp32 else torch.bfloat16
+    st = Lockstep(ll, 1, H, D, T, S, W, C, dtype)
     ll.ll_debug_pair_kernel(st.cache, pair)
     L = C * T
     for c in range(3):
-        q, k, v = (llsynth.seeded_normal(("stall", T, c, t), (L, H, D), device="cuda") for t in "qkv")
+        q, k, v = (llsynth.seeded_normal(("stall", T, c, t), (L, H, D), dtype=dtype, device="cuda") for t in "qkv")
         st.attend(0, q, k, v, commit=True, what="before the stall c%d" % c)
     state = ll.ll_cache_state(st.cache, 0)
-    q, k, v = (llsynth.seeded_normal(("stall-q", T, pair, t), (L, H, D), device="cuda") for t in "qkv")
+    q, k, v = (llsynth.seeded_normal(("stall-q", T, pair, t), (L, H, D), dtype=dtype, device="cuda")
+               for t in "qkv")
     ll.ll_debug_inject_stall(st.cache, True, 20000)  # 20 ms limit for the next launch's waits
     out = torch.empty_like(q)
     ll.ll_attend_chunk(st.cache, 0, q, k, v, out, False)  # enqueued fine; the device wait gives up
@@ -55,7 +60,7 @@ def test_stalled_wait_times_out_and_the_cache_keeps_working(ll, T, pair):
     # the context and the cache still work: the same pass again, then commits, against the oracle
     st.attend(0, q, k, v, commit=False, what="after the stall")
     for c in range(3, 5):
-        q, k, v = (llsynth.seeded_normal(("stall", T, c, t), (L, H, D), device="cuda") for t in "qkv")
+        q, k, v = (llsynth.seeded_normal(("stall", T, c, t), (L, H, D), dtype=dtype, device="cuda") for t in "qkv")
         st.attend(0, q, k, v, commit=True, what="after the stall c%d" % c)
     st.check_state()
     st.check_raw(0)

@@ -16,8 +16,9 @@
 // every cached key, and masks the chunk's own keys the same block-causal way
 // (the frame-causal chunk).
 //
-// This is the one-CTA form of the kernel, the one every bf16 attention runs on;
-// ll_attend_pair.cu holds a CTA-pair form for head_dim 128 (selected on request).
+// This is the one-CTA form of the kernel, the one every bf16 attention runs on
+// (and fp32 attention at head_dim 64, with tf32 operands); ll_attend_pair.cu
+// holds a CTA-pair form for head_dim 128 (selected on request).
 // Work item = one head x 256 query rows (two 128-row tiles that share every
 // K/V tile); one CTA per SM walks several items (see "Work schedule" in
 // ll_tc_common.cuh):
@@ -32,10 +33,22 @@
 //               P V product from two blocks of four (one per key half), with
 //               every descriptor ready in registers
 //   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: thread = row
-//   warps 2-3   idle
+//   warps 2-3   fp32 operands only: split each K tile into its tf32 part
+//               and the tf32 rounding of the remainder, and transpose each V
+//               tile into the K-major layout that P V reads (tf32 operands
+//               are taken K-major here); idle otherwise
 // Tensor memory (512 columns x 128 lanes): O0 [0,128) O1 [128,256)
 // S0 [256,384) S1 [384,512).  P (bf16) overwrites the first 64 columns of S
-// and feeds the P V product straight from tensor memory.
+// (fp32 operands: P rounded to tf32 overwrites all 128) and feeds the P V
+// product straight from tensor memory.
+// fp32 operands (head_dim 64): Q K^T is kept accurate to fp32 by splitting
+// each operand x into hi = tf32(x) and lo = tf32(x - hi) and summing three
+// tf32 products, S = Qhi Khi^T + Qlo Khi^T + Qhi Klo^T (the split-operand
+// "3xTF32" method; the dropped Qlo Klo^T is below 2^-22 of each product).  The
+// softmax threads split their Q rows (hi in place in shared memory, lo into
+// the unused columns [64,128) of their tile's O region, read by the MMA as A);
+// warps 2-3 split each K tile (hi in place, lo into a separate buffer).  P V
+// reads V rounded to tf32 and P rounded to tf32.
 // MMA order per key tile j: PV0(j) QK0(j+1) PV1(j) QK1(j+1), so the softmax of
 // one tile overlaps the tensor-core work of the other.  P of a tile is handed
 // over in two halves: once the P of keys 0-63 is in tensor memory the softmax
@@ -64,25 +77,36 @@ using namespace tc;
 constexpr int BM = 128;        // query rows per tile = TMEM lanes
 constexpr int BN = kKeyTile;   // keys per K/V tile
 constexpr int NQ = 2;          // query tiles per CTA
-constexpr int NS = 5;          // stages of the K/V tile ring
 constexpr int kThreads = 384;
 static_assert(NQ * BM == kItemRows, "a CTA takes one work item");
 
-// K8: Q and K in e4m3 (one byte per element; Q K^T on kind::f8f6f4), V in bf16.
-template <int D, bool K8>
+// Operand kinds: bf16 Q, K, V (kind::f16); e4m3 Q and K with bf16 V (Q K^T on
+// kind::f8f6f4); fp32 Q, K, V read by the tensor core as tf32 (kind::tf32).
+enum Kind : int { kBf16 = 0, kE4m3 = 1, kTf32 = 2 };
+
+template <int D, int KIND>
 struct Cfg {
-  static constexpr int kQKElem = K8 ? 1 : 2;                // bytes per Q / K element
+  static constexpr int kQKElem = KIND == kE4m3 ? 1 : KIND == kTf32 ? 4 : 2;  // bytes per Q / K element
+  static constexpr int kVElem = KIND == kTf32 ? 4 : 2;                        // bytes per V element
   static constexpr int kQKChunks = D * kQKElem / 128;       // 128-byte column chunks of Q and K
   static constexpr int kQKBox = 128 / kQKElem;              // elements per such chunk
-  static constexpr int kVChunks = D / 64;                   // 128-byte column chunks of V (bf16)
+  static constexpr int kVChunks = D * kVElem / 128;         // 128-byte column chunks of V
+  static constexpr int kVBox = 128 / kVElem;
   static constexpr int kKSteps = D * kQKElem / 32;          // 32-byte k-steps of one Q K^T product
   static constexpr int kKBytes = BN * D * kQKElem;          // one K tile
-  static constexpr int kVBytes = BN * D * 2;                // one V tile
+  static constexpr int kVBytes = BN * D * kVElem;           // one V tile
   static constexpr int kTileBytes = kVBytes;                // one ring stage (K or V)
   static constexpr int kQBytes = BM * D * kQKElem;          // one Q tile
+  static constexpr int kNS = KIND == kTf32 ? 3 : 5;         // stages of the K/V tile ring
+  static constexpr int kVTBytes = KIND == kTf32 ? kVBytes : 0;  // one V tile transposed (tf32)
+  static constexpr int kKLBytes = KIND == kTf32 ? kKBytes : 0;  // low parts of one K tile (tf32)
   static constexpr int kSmemKV = NQ * kQBytes;
-  static constexpr int kSmemBar = kSmemKV + NS * kTileBytes;
+  static constexpr int kSmemVT = kSmemKV + kNS * kTileBytes;
+  static constexpr int kSmemKL = kSmemVT + kVTBytes;
+  static constexpr int kSmemBar = kSmemKL + kKLBytes;
   static constexpr int kSmemBytes = kSmemBar + 256 + 1024;  // barriers, then alignment slack
+  static_assert(KIND != kTf32 || D == 64, "fp32 tiles fit the shared memory at head_dim 64 only");
+  static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
 };
 
 struct TcParams {
@@ -152,6 +176,52 @@ __device__ __forceinline__ void mma4_ss(uint32_t d, const uint64_t (&a)[4], cons
       "r"(idesc), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "r"(acc));
 }
 
+// Eight k-steps of kind::tf32 (8 fp32 elements per k-step), D (+)= A(smem) * B(smem);
+// k-step 0 accumulates when acc != 0.
+__device__ __forceinline__ void mma8_ss_tf32(uint32_t d, const uint64_t (&a)[8], const uint64_t (&b)[8],
+                                             uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p0, %18, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %2, %10, %1, p0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %3, %11, %1, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %4, %12, %1, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %5, %13, %1, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %6, %14, %1, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %7, %15, %1, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %8, %16, %1, p1;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], %9, %17, %1, p1;\n\t}" ::"r"(d),
+      "r"(idesc), "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]),
+      "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(acc));
+}
+// D(tmem) (+)= A(tmem: 8 k-steps of 8 tf32 columns from column a) * B(smem), kind::tf32
+__device__ __forceinline__ void mma8_ts_tf32(uint32_t d, uint32_t a, const uint64_t (&b)[8], uint32_t idesc,
+                                             uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p0, p1, e;\n\t.reg .b32 t;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p0, %11, 0;\n\tsetp.eq.b32 p1, 0, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [%2], %3, %1, p0;\n\t"
+      "add.u32 t, %2, 8;\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [t], %4, %1, p1;\n\t"
+      "add.u32 t, %2, 16;\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [t], %5, %1, p1;\n\t"
+      "add.u32 t, %2, 24;\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [t], %6, %1, p1;\n\t"
+      "add.u32 t, %2, 32;\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [t], %7, %1, p1;\n\t"
+      "add.u32 t, %2, 40;\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [t], %8, %1, p1;\n\t"
+      "add.u32 t, %2, 48;\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [t], %9, %1, p1;\n\t"
+      "add.u32 t, %2, 56;\n\t@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [t], %10, %1, p1;\n\t}" ::"r"(d),
+      "r"(idesc), "r"(a), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
+      "r"(acc));
+}
+// fp32 -> tf32, round to nearest (ties away from zero); the low 13 bits come out zero
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return r;
+}
+// x = hi + lo + (below 2^-22 |x|): hi = tf32(x), lo = tf32(x - hi) (x - hi is exact in fp32)
+__device__ __forceinline__ void split_tf32(float x, float& hi, float& lo) {
+  hi = __uint_as_float(to_tf32(x));
+  lo = __uint_as_float(to_tf32(x - hi));
+}
+
 // D(tmem) (+)= A(tmem: 4 k-steps of 8 columns from column a) * B(smem), elected lane
 __device__ __forceinline__ void mma4_ts(uint32_t d, uint32_t a, const uint64_t (&b)[4], uint32_t idesc, uint32_t acc) {
   asm volatile(
@@ -167,15 +237,18 @@ __device__ __forceinline__ void mma4_ts(uint32_t d, uint32_t a, const uint64_t (
 // ----------------------------------------------------------------------------
 // The kernel
 // ----------------------------------------------------------------------------
-template <int D, bool K8>
+template <int D, int KIND>
 __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_constant__ TcParams p) {
-  using Cf = Cfg<D, K8>;
+  using Cf = Cfg<D, KIND>;
+  constexpr int NS = Cf::kNS;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sQ = base;
   const uint32_t sKV = base + Cf::kSmemKV;
+  const uint32_t sVT = base + Cf::kSmemVT;  // fp32 operands: the V tile P V reads, K-major
+  const uint32_t sKL = base + Cf::kSmemKL;  // fp32 operands: low parts of the K tile
   const uint32_t sBar = base + Cf::kSmemBar;
   const uint32_t bQfull = sBar;
   const uint32_t bQempty = sBar + 8;
@@ -186,7 +259,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
   const uint32_t bOfull = bP0 + 32;  // bP0: P of keys 0-63 of tile w at +8w, of keys 64-127 at +16+8w
   const uint32_t bOempty = bOfull + 8;
   const uint32_t bDrain = bOempty + 8;
-  constexpr int kBarBytes = 16 + 16 * NS + 16 + 32 + 24;
+  const uint32_t bVTfull = bDrain + 8;    // fp32 operands: V tile transposed
+  const uint32_t bVTempty = bDrain + 16;  // fp32 operands: P V of both query tiles done with it
+  const uint32_t bKsplit = bDrain + 24;   // fp32 operands: K tile split (hi in place, lo in sKL)
+  const uint32_t bKLempty = bDrain + 32;  // fp32 operands: Q K^T of both query tiles done with sKL
+  const uint32_t bQsplit = bDrain + 40;   // fp32 operands: both Q tiles split
+  constexpr int kBarBytes = 16 + 16 * NS + 16 + 32 + 24 + 40;
   static_assert(kBarBytes + 8 <= 256, "barrier area");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Cf::kSmemBar + kBarBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Cf::kSmemBar + kBarBytes + 4);
@@ -210,6 +288,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     mbar_init(bOfull, 1);
     mbar_init(bOempty, NQ * 128);
     mbar_init(bDrain, 1);
+    mbar_init(bVTfull, 64);
+    mbar_init(bVTempty, 1);
+    mbar_init(bKsplit, 64);
+    mbar_init(bKLempty, 1);
+    mbar_init(bQsplit, NQ * 128);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -255,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
             mbar_expect_tx(full, is_v ? Cf::kVBytes : Cf::kKBytes);
             const uint32_t dst = sKV + s * Cf::kTileBytes;
             const int nc = is_v ? Cf::kVChunks : Cf::kQKChunks;
-            const int cw = is_v ? 64 : Cf::kQKBox;  // elements per 128-byte chunk
+            const int cw = is_v ? Cf::kVBox : Cf::kQKBox;  // elements per 128-byte chunk
             if (j < nA) {
               const CUtensorMap* m = is_v ? &p.tm_vc : &p.tm_kc;
               for (int c = 0; c < nc; ++c) tma_load_3d(dst + c * kAtom, m, full, c * cw, j * BN, head);
@@ -271,8 +354,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
   } else if (warp == 1) {
     {
       // ------------------------------ MMA issuer (whole warp) --------------------
-      constexpr uint32_t kIdQK = K8 ? idesc_e4m3(BM, BN) : idesc_bf16(BM, BN, 0, 0);  // Q, K both K-major
-      constexpr uint32_t kIdPV = idesc_bf16(BM, D, 0, 1);   // P from TMEM; V is N(=d)-major
+      // Q, K both K-major
+      constexpr uint32_t kIdQK = KIND == kE4m3   ? idesc_e4m3(BM, BN)
+                                 : KIND == kTf32 ? idesc_tf32(BM, BN)
+                                                 : idesc_bf16(BM, BN, 0, 0);
+      // P from TMEM; V is N(=d)-major, or K-major after the transpose (tf32)
+      constexpr uint32_t kIdPV = KIND == kTf32 ? idesc_tf32(BM, D) : idesc_bf16(BM, D, 0, 1);
       // The tensor core takes one 128x128x16 MMA per 64 clocks, but this warp
       // shares its SMSP's issue slots with two busy softmax warps and gets few of
       // them, so each MMA group must cost it as few instructions as possible.
@@ -299,25 +386,50 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       const uint64_t dV0 = sw128_desc(sKV, kAtom, 1024);
       const uint32_t k_lo0 = (uint32_t)dK0, k_hi = (uint32_t)(dK0 >> 32);
       const uint32_t v_lo0 = (uint32_t)dV0, v_hi = (uint32_t)(dV0 >> 32);
+      // tf32: the transposed V tile sits at one address; k-step ks (8 keys, 32
+      // bytes) lies in the 128-byte column chunk ks / 4, whose D rows take D * 128 bytes
+      // (the low parts of a K tile sit at one address too, laid out as the K tile)
+      uint64_t dvt0[8], dvt1[8], dkl[8];
+      if constexpr (KIND == kTf32) {
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          dvt0[ks] = sw128_desc(sVT + (ks >> 2) * (D * 128) + (ks & 3) * 32, 16, 1024);
+          dvt1[ks] = sw128_desc(sVT + ((ks + 8) >> 2) * (D * 128) + (ks & 3) * 32, 16, 1024);
+          dkl[ks] = sw128_desc(sKL + (ks >> 2) * kAtom + (ks & 3) * 32, 16, 1024);
+        }
+      }
       auto issue_qk = [&](int w, int stage) {
         const uint32_t lo = k_lo0 + (((uint32_t)stage * Cf::kTileBytes) >> 4);
         uint64_t bd[KS];
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) bd[ks] = make_desc(lo + ((ks >> 2) * kAtom + (ks & 3) * 32) / 16, k_hi);
-        if constexpr (K8)
+        if constexpr (KIND == kE4m3)
           mma4_ss_f8(tmem + 256 + 128 * w, dq[w], bd, kIdQK);
+        else if constexpr (KIND == kTf32) {
+          const uint32_t sd = tmem + 256 + 128 * w;
+          mma8_ss_tf32(sd, dq[w], bd, kIdQK, 0u);                // Qhi Khi^T
+          mma8_ts_tf32(sd, tmem + 64 + 128 * w, bd, kIdQK, 1u);  // Qlo Khi^T, Qlo in tensor memory
+          mma8_ss_tf32(sd, dq[w], dkl, kIdQK, 1u);               // Qhi Klo^T
+        }
         else if constexpr (KS == 8)
           mma8_ss(tmem + 256 + 128 * w, dq[w], bd, kIdQK, 0u);
         else
           mma4_ss(tmem + 256 + 128 * w, dq[w], bd, kIdQK, 0u);
       };
-      // P V in two groups of four k-steps: keys 0-63, then keys 64-127
+      // P V in two groups of k-steps: keys 0-63, then keys 64-127
       auto issue_pv = [&](int w, int stage, int half, bool acc) {
-        const uint32_t lo = v_lo0 + (((uint32_t)stage * Cf::kTileBytes) >> 4);
-        uint64_t bd[4];
+        if constexpr (KIND == kTf32) {
+          uint64_t bd[8];
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) bd[ks] = make_desc(lo + ((half * 4 + ks) * 16 * 128) / 16, v_hi);
-        mma4_ts(tmem + 128 * w, tmem + 256 + 128 * w + 32 * half, bd, kIdPV, acc ? 1u : 0u);
+          for (int ks = 0; ks < 8; ++ks) bd[ks] = half ? dvt1[ks] : dvt0[ks];
+          mma8_ts_tf32(tmem + 128 * w, tmem + 256 + 128 * w + 64 * half, bd, kIdPV, acc ? 1u : 0u);
+        } else {
+          const uint32_t lo = v_lo0 + (((uint32_t)stage * Cf::kTileBytes) >> 4);
+          uint64_t bd[4];
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) bd[ks] = make_desc(lo + ((half * 4 + ks) * 16 * 128) / 16, v_hi);
+          mma4_ts(tmem + 128 * w, tmem + 256 + 128 * w + 32 * half, bd, kIdPV, acc ? 1u : 0u);
+        }
       };
       Walker wk;
       walker_init(wk, p.a, p.s, blockIdx.x);
@@ -328,12 +440,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         const int n = pc.j1 - pc.j0;
         if (!(ok = __all_sync(0xffffffffu, wait(bQfull, qi & 1, ctl)))) break;
         if (!(ok = __all_sync(0xffffffffu, wait(bKVfull0 + 8 * (u % NS), (u / NS) & 1, ctl)))) break;
+        if constexpr (KIND == kTf32) {
+          if (!(ok = __all_sync(0xffffffffu, wait(bQsplit, qi & 1, ctl)))) break;
+          if (!(ok = __all_sync(0xffffffffu, wait(bKsplit, jt & 1, ctl)))) break;
+        }
         tc_fence_after();
         issue_qk(0, u % NS);
         tc_commit_e(bS0);
         issue_qk(1, u % NS);
         tc_commit_e(bS0 + 8);
         tc_commit_e(bKVempty0 + 8 * (u % NS));
+        if constexpr (KIND == kTf32) tc_commit_e(bKLempty);
         if (n == 1) tc_commit_e(bQempty);
         for (int t = 0; t < n; ++t) {
           const int uv = u + 2 * t + 1, sv = uv % NS;
@@ -341,6 +458,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
           const bool more = t + 1 < n;
           if (!(ok = __all_sync(0xffffffffu, wait(bKVfull0 + 8 * sv, (uv / NS) & 1, ctl)))) break;
           if (!(ok = __all_sync(0xffffffffu, wait(bP0, (jt + t) & 1, ctl)))) break;
+          if constexpr (KIND == kTf32) {
+            if (!(ok = __all_sync(0xffffffffu, wait(bVTfull, (jt + t) & 1, ctl)))) break;
+          }
           // the previous item's epilogue must have read O out of tensor memory
           if (t == 0 && qi > 0 && !(ok = __all_sync(0xffffffffu, wait(bOempty, (qi - 1) & 1, ctl)))) break;
           tc_fence_after();
@@ -350,6 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
           issue_pv(0, sv, 1, true);
           if (more) {
             if (!(ok = __all_sync(0xffffffffu, wait(bKVfull0 + 8 * sk, (uk / NS) & 1, ctl)))) break;
+            if constexpr (KIND == kTf32) {
+              if (!(ok = __all_sync(0xffffffffu, wait(bKsplit, (jt + t + 1) & 1, ctl)))) break;
+            }
             tc_fence_after();
             issue_qk(0, sk);
             tc_commit_e(bS0);
@@ -361,10 +484,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
           tc_fence_after();
           issue_pv(1, sv, 1, true);
           tc_commit_e(bKVempty0 + 8 * sv);
+          if constexpr (KIND == kTf32) tc_commit_e(bVTempty);
           if (more) {
             issue_qk(1, sk);
             tc_commit_e(bS0 + 8);
             tc_commit_e(bKVempty0 + 8 * sk);
+            if constexpr (KIND == kTf32) tc_commit_e(bKLempty);
             if (t + 2 == n) tc_commit_e(bQempty);
           }
         }
@@ -373,6 +498,78 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         u += 2 * n;
         jt += n;
         ++qi;
+      }
+    }
+  } else if (warp < 4) {
+    if constexpr (KIND == kTf32) {
+      // ------------------------------ K split, V transpose (fp32 operands) -------
+      // Per key tile, in the order the producer loads them:
+      // K: each element x becomes hi = tf32(x) in place and lo = tf32(x - hi) at
+      //    the same offset of the low-part buffer (same layout as the K tile).
+      // V: TMA leaves a V tile as key rows: column chunk c holds d in [32c, 32c+32)
+      //    of every key, 128 bytes per key, its 16-byte units swizzled by key % 8.
+      //    P V reads it K-major, rounded to tf32: rows of d, column chunks of 32
+      //    keys (D rows x 128 bytes each), 16-byte units swizzled by d % 8.  Each
+      //    warp instruction moves one 16-byte unit of 32 consecutive keys, so
+      //    neither the loads nor the 4-byte stores meet a bank conflict.
+      const int tt = threadIdx.x - 64;
+      uint8_t* vt = gbase + Cf::kSmemVT;
+      uint8_t* kl = gbase + Cf::kSmemKL;
+      constexpr int kUnits = BN * D / 4;  // 16-byte units of a K or V tile
+      Walker wk;
+      walker_init(wk, p.a, p.s, blockIdx.x);
+      Piece pc;
+      int u = 0, ti = 0;
+      bool ok = true;
+      while (ok && walker_next(wk, p.a, p.s, pc, blockIdx.x)) {
+        const int n = pc.j1 - pc.j0;
+        for (int t = 0; t < n; ++t, ++ti) {
+          const int uk = u + 2 * t, sk = uk % NS;
+          if (!(ok = wait(bKVfull0 + 8 * sk, (uk / NS) & 1, ctl))) break;
+          // Q K^T of the previous tile (both query tiles) is done with the low parts
+          if (ti > 0 && !(ok = wait(bKLempty, (ti - 1) & 1, ctl))) break;
+          uint8_t* kt = gbase + Cf::kSmemKV + sk * Cf::kTileBytes;
+#pragma unroll 4
+          for (int x = tt; x < kUnits; x += 64) {
+            float4* ph = reinterpret_cast<float4*>(kt + 16 * x);
+            float4* pl = reinterpret_cast<float4*>(kl + 16 * x);
+            const float4 val = *ph;
+            float4 hi, lo;
+            split_tf32(val.x, hi.x, lo.x);
+            split_tf32(val.y, hi.y, lo.y);
+            split_tf32(val.z, hi.z, lo.z);
+            split_tf32(val.w, hi.w, lo.w);
+            *ph = hi;
+            *pl = lo;
+          }
+          // generic-proxy writes, read by the tensor core (async proxy)
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive(bKsplit);
+
+          const int uv = uk + 1, sv = uv % NS;
+          if (!(ok = wait(bKVfull0 + 8 * sv, (uv / NS) & 1, ctl))) break;
+          // P V of the previous tile (both query tiles) is done with the buffer
+          if (ti > 0 && !(ok = wait(bVTempty, (ti - 1) & 1, ctl))) break;
+          const uint8_t* raw = gbase + Cf::kSmemKV + sv * Cf::kTileBytes;
+#pragma unroll 4
+          for (int x = tt; x < kUnits; x += 64) {
+            const int k = x % BN;
+            const int c = (x / BN) >> 3, q4 = (x / BN) & 7;
+            const float4 val = *reinterpret_cast<const float4*>(raw + c * kAtom + k * 128 + ((q4 ^ (k & 7)) << 4));
+            const float e4[4] = {val.x, val.y, val.z, val.w};
+            uint8_t* col = vt + (k >> 5) * (D * 128) + (k & 3) * 4;
+            const int ku = (k & 31) >> 2;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int d = c * 32 + q4 * 4 + e;
+              *reinterpret_cast<uint32_t*>(col + d * 128 + ((ku ^ (d & 7)) << 4)) = to_tf32(e4[e]);
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive(bVTfull);
+        }
+        if (!ok) break;
+        u += 2 * n;
       }
     }
   } else if (warp >= 4) {
@@ -402,6 +599,40 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         row_end = (int)(e < a.Lb ? e : a.Lb);
       }
       const int n = pc.j1 - pc.j0;
+      if constexpr (KIND == kTf32) {
+        // split this thread's Q row: hi in place (Q K^T reads it from shared
+        // memory), lo into columns [64, 128) of the tile's O region (read as A
+        // from tensor memory); the previous piece's Q K^T products are done with
+        // both, since the producer reloads Q only after they complete
+        ok = __all_sync(0xffffffffu, wait(bQfull, qi & 1, ctl));
+        if (!ok) break;
+        uint8_t* qs = gbase + w * Cf::kQBytes + row * 128;
+        uint32_t qlo[D];
+#pragma unroll
+        for (int c = 0; c < Cf::kQKChunks; ++c)
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            float4* ph = reinterpret_cast<float4*>(qs + c * kAtom + ((q4 ^ (row & 7)) << 4));
+            const float4 val = *ph;
+            float4 hi, lo;
+            split_tf32(val.x, hi.x, lo.x);
+            split_tf32(val.y, hi.y, lo.y);
+            split_tf32(val.z, hi.z, lo.z);
+            split_tf32(val.w, hi.w, lo.w);
+            *ph = hi;
+            const int d = c * 32 + q4 * 4;
+            qlo[d] = __float_as_uint(lo.x);
+            qlo[d + 1] = __float_as_uint(lo.y);
+            qlo[d + 2] = __float_as_uint(lo.z);
+            qlo[d + 3] = __float_as_uint(lo.w);
+          }
+#pragma unroll
+        for (int cc = 0; cc < D / 16; ++cc) tmem_st16(tO + 64 + 16 * cc, qlo + 16 * cc);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bQsplit);
+      }
       float m = -INFINITY, l = 0.f;
       for (int t = 0; t < n; ++t) {
         const int j = pc.j0 + t;
@@ -447,6 +678,30 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         // packed P word directly (exact widening, fp32 add)
         const uint64_t sl2x2 = pack_f32x2(sl2, sl2), nmo2 = pack_f32x2(-mo, -mo);
         float ls[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if constexpr (KIND == kTf32) {
+          // P rounded to tf32 (what P V reads), one fp32 column per key; the row
+          // sum adds the same rounded values
+#pragma unroll
+          for (int g = 0; g < BN / 16; ++g) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int c = g * 16 + 2 * i;
+              float x0, x1;
+              fma_f32x2(x0, x1, __uint_as_float(r[c]), __uint_as_float(r[c + 1]), sl2x2, nmo2);
+              pk[2 * i] = to_tf32(ex2(x0));
+              pk[2 * i + 1] = to_tf32(ex2(x1));
+              ls[2 * (i & 3)] += __uint_as_float(pk[2 * i]);
+              ls[2 * (i & 3) + 1] += __uint_as_float(pk[2 * i + 1]);
+            }
+            tmem_st16(tS + 16 * g, pk);
+            if (g == 3 && !rescale) {
+              tmem_st_wait();
+              tc_fence_before();
+              if (!(a.stall_inject && jt + t == 0 && w == 0)) mbar_arrive(bP);
+            }
+          }
+        } else {
 #pragma unroll
         for (int g = 0; g < BN / 32; ++g) {
           uint32_t pk[16];
@@ -466,6 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
             tc_fence_before();
             if (!(a.stall_inject && jt + t == 0 && w == 0)) mbar_arrive(bP);
           }
+        }
         }
         l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
         if (rescale) {
@@ -576,16 +832,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
   }
 }
 
-template <int D, bool K8>
+template <int D, int KIND>
 cudaError_t launch_tc(const AttendArgs& a, cudaStream_t stream) {
-  constexpr int qk = K8 ? 1 : 2;  // bytes per Q / K element
+  constexpr int qk = Cfg<D, KIND>::kQKElem, ve = Cfg<D, KIND>::kVElem;  // bytes per element
   TcParams p;
   std::memset(&p, 0, sizeof(p));
   p.a = a;
   if (!encode_tokens(&p.tm_q, a.q, a.Lq, a.heads, D, BM, qk) ||
-      !encode_tokens(&p.tm_kn, a.kn, a.Lb, a.heads, D, BN, qk) || !encode_tokens(&p.tm_vn, a.vn, a.Lb, a.heads, D, BN) ||
+      !encode_tokens(&p.tm_kn, a.kn, a.Lb, a.heads, D, BN, qk) ||
+      !encode_tokens(&p.tm_vn, a.vn, a.Lb, a.heads, D, BN, ve) ||
       !encode_cache(&p.tm_kc, a.kc, a.La, a.heads, D, a.cache_head_elems, BN, qk) ||
-      !encode_cache(&p.tm_vc, a.vc, a.La, a.heads, D, a.cache_head_elems, BN))
+      !encode_cache(&p.tm_vc, a.vc, a.La, a.heads, D, a.cache_head_elems, BN, ve))
     return cudaErrorInvalidValue;
   p.s.nqb = (a.Lq + NQ * BM - 1) / (NQ * BM);
   CombineParams cp;
@@ -604,8 +861,8 @@ cudaError_t launch_tc(const AttendArgs& a, cudaStream_t stream) {
     p.part = a.scratch;
   }
   static std::atomic<int> attr_done[64];
-  if (cudaError_t e = smem_opt_in(attend_tc_kernel<D, K8>, Cfg<D, K8>::kSmemBytes, attr_done)) return e;
-  attend_tc_kernel<D, K8><<<(unsigned)p.s.grid, kThreads, Cfg<D, K8>::kSmemBytes, stream>>>(p);
+  if (cudaError_t e = smem_opt_in(attend_tc_kernel<D, KIND>, Cfg<D, KIND>::kSmemBytes, attr_done)) return e;
+  attend_tc_kernel<D, KIND><<<(unsigned)p.s.grid, kThreads, Cfg<D, KIND>::kSmemBytes, stream>>>(p);
   count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || cp.nsplit == 0) return e;
@@ -680,9 +937,13 @@ int attend_schedule_dump(int Lq, int La, int Lb, int heads, int max_ctas, int mo
 }
 
 cudaError_t launch_attend_bf16_tc(const AttendArgs& a, cudaStream_t stream) {
-  if (a.qk_fp8) return a.head_dim == 128 ? launch_tc<128, true>(a, stream) : cudaErrorInvalidValue;
-  if (a.head_dim == 64) return launch_tc<64, false>(a, stream);
-  return a.pair ? launch_attend_bf16_pair(a, stream) : launch_tc<128, false>(a, stream);
+  if (a.qk_fp8) return a.head_dim == 128 ? launch_tc<128, kE4m3>(a, stream) : cudaErrorInvalidValue;
+  if (a.head_dim == 64) return launch_tc<64, kBf16>(a, stream);
+  return a.pair ? launch_attend_bf16_pair(a, stream) : launch_tc<128, kBf16>(a, stream);
+}
+
+cudaError_t launch_attend_tf32_tc(const AttendArgs& a, cudaStream_t stream) {
+  return a.head_dim == 64 ? launch_tc<64, kTf32>(a, stream) : cudaErrorInvalidValue;
 }
 
 }  // namespace ll

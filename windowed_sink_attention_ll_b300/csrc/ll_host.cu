@@ -235,8 +235,12 @@ ll_status launch_attend(ll_cache* c, const ll::AttendArgs& a, cudaStream_t st, i
     a8.q = c->q8;
     a8.kn = c->k8;
     if (e == cudaSuccess) e = ll::launch_attend_bf16_tc(a8, st);
-  } else if (c->dtype == LL_FP32 || c->use_simt) {
+  } else if (c->use_simt || (c->dtype == LL_FP32 && c->D != 64)) {
+    // the CUDA-core kernel: fp32 at head_dim 128 (two fp32 query tiles and a K/V
+    // ring do not fit one CTA's shared memory), or on request (tests)
     e = ll::launch_attend_simt(a, c->eb, st);
+  } else if (c->dtype == LL_FP32) {
+    e = ll::launch_attend_tf32_tc(a, st);
   } else {
     e = ll::launch_attend_bf16_tc(a, st);
   }
@@ -394,7 +398,7 @@ ll_status ll_cache_create(ll_cache** out, int layers, int heads, int head_dim, i
   const int fill = c->poison ? 0xFF : 0;
   if (cudaMemset(c->k, fill, kbytes) != cudaSuccess || cudaMemset(c->v, fill, vbytes) != cudaSuccess)
     return fail(LL_ERR_CUDA);
-  if (dtype != LL_FP32) {
+  if (dtype != LL_FP32 || head_dim == 64) {
     // the tensor-core kernel splits left-over work items across SMs and merges
     // their partial results: two slots per SM
     c->scratch_slots = ll::attend_scratch_slots_wanted();

@@ -82,6 +82,8 @@ struct AttendArgs {
 // a.pair the CTA-pair kernel.
 cudaError_t launch_attend_bf16_tc(const AttendArgs& a, cudaStream_t stream);
 cudaError_t launch_attend_bf16_pair(const AttendArgs& a, cudaStream_t stream);
+// fp32 attention on the tensor cores (tf32 operands), head_dim 64.
+cudaError_t launch_attend_tf32_tc(const AttendArgs& a, cudaStream_t stream);
 // Scratch of the tensor-core kernel: bytes for `slots` partial results, and the
 // slot count it uses on the current device (two per SM).
 size_t attend_scratch_bytes(int head_dim, int slots);

@@ -202,6 +202,11 @@ __device__ __forceinline__ uint64_t make_desc(uint32_t lo, uint32_t hi) {
 __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
   return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
+// Instruction descriptor, kind::tf32: tf32 A and B (format code 2), fp32 D, M x N,
+// both operands K-major.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+  return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M x N, A/B major-ness.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
@@ -456,8 +461,8 @@ inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return f;
 }
 
-// 3-D tensor map of bf16 (elem_bytes 2) or byte-sized e4m3 (elem_bytes 1) elements,
-// 128-byte swizzle
+// 3-D tensor map of bf16 (elem_bytes 2), byte-sized e4m3 (elem_bytes 1) or fp32
+// (elem_bytes 4) elements, 128-byte swizzle
 inline bool encode3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t s1,
                      uint64_t s2, uint32_t b0, uint32_t b1, uint32_t b2, int elem_bytes = 2) {
   auto fn = encode_fn();
@@ -466,7 +471,9 @@ inline bool encode3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1,
   cuuint64_t strides[2] = {s1, s2};
   cuuint32_t box[3] = {b0, b1, b2};
   cuuint32_t es[3] = {1, 1, 1};
-  const CUtensorMapDataType dt = elem_bytes == 1 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapDataType dt = elem_bytes == 1   ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                 : elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                                   : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
