@@ -374,19 +374,24 @@ def timed_region(args, world, local, caches, step, profile_every=1):
 
 
 def attend_kernel_name(args):
+    if args.kv_fp8:
+        return "attend_tc_kernel<128, e4m3 keys and values>"
     if args.key_fp8:
         return "attend_tc_kernel<128, e4m3 keys>"
     return "attend_pair_kernel (CTA pair)" if args.pair else "attend_tc_kernel<128>"
 
 
 def cache_dtype(ll, args):
+    if args.kv_fp8:
+        return ll.LL_FP8
     return ll.LL_BF16_K8 if args.key_fp8 else ll.LL_BF16
 
 
 def peak_scale(args):
     """Tensor peak of the attention relative to the bf16 peak.  With e4m3 keys Q K^T (half
     the flops) runs at the FP8 rate, twice the bf16 rate (the nominal ratio, 4.5 / 2.25
-    PFLOP/s), and P V at the bf16 rate: 1 / (0.5 / 2 + 0.5 / 1) = 4 / 3."""
+    PFLOP/s), and P V at the bf16 rate: 1 / (0.5 / 2 + 0.5 / 1) = 4 / 3.  With e4m3 values
+    as well P V runs on fp16 operands, at the same rate as bf16: 4 / 3 again."""
     return 4.0 / 3.0 if args.key_fp8 else 1.0
 
 
@@ -419,7 +424,8 @@ def base_result(args, world, value, ms_max, config):
     return {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (keys e4m3)" if args.key_fp8 else "bf16",
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 (keys and values e4m3)" if args.kv_fp8 else "bf16 (keys e4m3)" if args.key_fp8 else "bf16",
         "data": "synthetic (seeded N(0,1) q/k/v per layer and chunk, Wan2.1-1.3B shapes; no weights)",
         "config": config,
     }
@@ -882,6 +888,9 @@ def main():
                     help="resident (default): recache rewrites sink and window; window: the sink keeps its K/V")
     ap.add_argument("--key-fp8", action="store_true",
                     help="an FP8-key cache (LL_BF16_K8): keys stored in e4m3, Q K^T at the FP8 tensor rate")
+    ap.add_argument("--kv-fp8", action="store_true",
+                    help="an FP8 cache (LL_FP8): keys and values stored in e4m3, Q K^T at the FP8 tensor rate, "
+                         "P V on fp16 operands")
     ap.add_argument("--pair", action="store_true",
                     help="run head_dim 128 on the CTA-pair tensor-core kernel instead of the default one-CTA kernel")
     ap.add_argument("--ref-budget-s", type=float, default=None,
@@ -891,6 +900,7 @@ def main():
     ap.add_argument("--e2e-streams", type=int, default=3, help="host-to-device copy streams of the e2e measurement")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
+    args.key_fp8 = args.key_fp8 or args.kv_fp8  # an FP8 cache stores its keys in e4m3 too
     if args.warmup < 3:
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":

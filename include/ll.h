@@ -68,8 +68,13 @@ typedef struct ll_cache ll_cache; /* opaque */
  *     takes half the bytes.  head_dim 128 only.  (The pages report INT8
  *     inference (Abstract, §5 Conclusion); rounding the keys is a defined input
  *     step, so results match attention over the rounded q and k.)
+ *   LL_FP8: as LL_BF16_K8, and the V cache holds every value rounded to e4m3
+ *     the same way: both caches take half the bytes of bf16.  P V runs on the
+ *     tensor cores with fp16 operands (kind::f16): each V tile is widened to
+ *     fp16 (exact for e4m3) in shared memory and P is rounded to fp16.  Results
+ *     match attention over the rounded q, k and v.  head_dim 128 only.
  */
-typedef enum { LL_BF16 = 0, LL_FP32 = 1, LL_BF16_K8 = 2 } ll_dtype;
+typedef enum { LL_BF16 = 0, LL_FP32 = 1, LL_BF16_K8 = 2, LL_FP8 = 3 } ll_dtype;
 
 typedef enum {
   LL_OK = 0,
@@ -89,11 +94,12 @@ LL_API const char* ll_status_str(ll_status s);
  * §3.3 "Short window attention": the cache is sized by the window, not by the
  * video length: K and V each hold layers * H * (S + W) * T * d elements,
  * head-major [layer][head][slot][token][d] (K one byte per element with
- * LL_BF16_K8).  The memory is cudaMalloc'ed on the current device and
+ * LL_BF16_K8, K and V with LL_FP8).  The memory is cudaMalloc'ed on the
+ * current device and
  * zero-filled; ll_cache_destroy frees it.
  * Requirements: layers, heads, tokens_per_frame, chunk_frames >= 1;
  * sink_frames, window_frames >= 0; head_dim in {64, 128} (128 for
- * LL_BF16_K8).  Limits of the
+ * LL_BF16_K8 and LL_FP8).  Limits of the
  * library, beyond which the call returns LL_ERR_UNSUPPORTED: S + W <= 512 and
  * C <= 512 frames, heads <= 127 (the commit copy runs 512 x heads blocks at
  * most), (S + W + C) * T <= 2^30 tokens.  Returns LL_ERR_OOM if the
@@ -207,7 +213,7 @@ LL_API ll_status ll_cache_state(ll_cache* cache, int layer, int64_t* frames_comm
  * ll_cache_read -- copy one layer's raw cache to HOST buffers, each
  * H * (S + W) * T * d elements in the head-major slot layout (for tests;
  * synchronises the device).  With LL_BF16_K8 host_k receives the e4m3 bytes
- * (one per element) and host_v bf16.
+ * (one per element) and host_v bf16; with LL_FP8 both receive e4m3 bytes.
  */
 LL_API ll_status ll_cache_read(ll_cache* cache, int layer, void* host_k, void* host_v);
 
@@ -215,7 +221,8 @@ LL_API ll_status ll_cache_read(ll_cache* cache, int layer, void* host_k, void* h
 LL_API ll_status ll_sync(ll_cache* cache);
 
 /* Sizes of a cache: S + W slots, bytes of one layer's K cache and the size of a K element
- * (V: the same, except LL_BF16_K8, whose V elements take 2 bytes and K elements 1). */
+ * (V: the same, except LL_BF16_K8, whose V elements take 2 bytes and K elements 1).
+ * With LL_FP8 K and V elements both take 1 byte. */
 LL_API ll_status ll_cache_info(const ll_cache* cache, int* slots, size_t* layer_bytes, int* elem_bytes);
 
 /*
@@ -264,8 +271,8 @@ LL_API ll_status ll_debug_inject_stall(ll_cache* cache, int enable, int timeout_
  * Test hook: a non-zero value routes this cache's bf16 or fp32 attention
  * through the CUDA-core kernel (one warp per query row; the one fp32 at
  * head_dim 128 runs on) instead of the tensor-core kernel, so tests can compare
- * the two CUDA kernels.  An LL_BF16_K8 cache ignores it (its keys need the FP8
- * tensor-core path).
+ * the two CUDA kernels.  LL_BF16_K8 and LL_FP8 caches ignore it (their keys need
+ * the FP8 tensor-core path).
  */
 LL_API ll_status ll_debug_use_simt(ll_cache* cache, int enable);
 
@@ -274,7 +281,7 @@ LL_API ll_status ll_debug_use_simt(ll_cache* cache, int enable);
  * through the CTA-pair tensor-core kernel (two SMs share every MMA, M = 256;
  * slower than the default one-CTA kernel on B300) instead of the one-CTA
  * kernel, so tests and benchmarks can run both on the same inputs.  Other
- * head dims and LL_BF16_K8 caches ignore it.
+ * head dims and the e4m3 caches (LL_BF16_K8, LL_FP8) ignore it.
  */
 LL_API ll_status ll_debug_pair_kernel(ll_cache* cache, int enable);
 

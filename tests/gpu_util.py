@@ -82,8 +82,8 @@ def bits(t: torch.Tensor) -> torch.Tensor:
 
 
 def round_e4m3(t: torch.Tensor) -> torch.Tensor:
-    """bf16 values rounded to FP8 e4m3 as the library rounds keys and queries for an
-    LL_BF16_K8 cache: nearest value, ties to even, saturating at +-448 (torch's own
+    """bf16 values rounded to FP8 e4m3 as the library rounds keys and queries for the
+    e4m3 caches (and values for LL_FP8): nearest value, ties to even, saturating at +-448 (torch's own
     conversion returns NaN past 480, hence the clamp).  Returns a float8_e4m3fn CPU tensor."""
     return torch.clamp(t.detach().cpu().float(), -448.0, 448.0).to(torch.float8_e4m3fn)
 
@@ -98,12 +98,16 @@ class Lockstep:
     (CPU tensors), so the raw cache bytes can be compared slot by slot.
     """
 
-    def __init__(self, ll, layers, heads, head_dim, T, S, W, C, dtype, keep_frames=True, key_fp8=False):
+    def __init__(self, ll, layers, heads, head_dim, T, S, W, C, dtype, keep_frames=True, key_fp8=False,
+                 value_fp8=False):
         """key_fp8: an LL_BF16_K8 cache (bf16 tokens, e4m3 key cache); the oracle is fed q and k
-        rounded to e4m3 as the library rounds them, and the raw K slots hold e4m3 bytes."""
+        rounded to e4m3 as the library rounds them, and the raw K slots hold e4m3 bytes.
+        value_fp8: an LL_FP8 cache (e4m3 keys and values): v is rounded the same way too."""
         self.ll = ll
-        self.key_fp8 = key_fp8
-        self.cache = ll.ll_cache_create(layers, heads, head_dim, T, S, W, C, ll.LL_BF16_K8 if key_fp8 else dtype)
+        self.key_fp8 = key_fp8 or value_fp8
+        self.value_fp8 = value_fp8
+        code = ll.LL_FP8 if value_fp8 else ll.LL_BF16_K8 if key_fp8 else dtype
+        self.cache = ll.ll_cache_create(layers, heads, head_dim, T, S, W, C, code)
         # slots without a resident frame hold NaN bytes, so a read of one would show in the outputs
         ll.ll_debug_poison(self.cache, True)
         self.orc = oracle.OracleCache(layers, heads, head_dim, T, S, W, C)
@@ -130,21 +134,29 @@ class Lockstep:
         """What the K cache stores for keys k (CPU): the e4m3 bytes for an FP8-key cache."""
         return round_e4m3(k).view(torch.uint8) if self.key_fp8 else k.cpu()
 
+    def v64(self, t):
+        """v as the oracle sees it: rounded to e4m3 first for an LL_FP8 cache."""
+        return f64(round_e4m3(t)) if self.value_fp8 else f64(t)
+
+    def value_store(self, v):
+        """What the V cache stores for values v (CPU): the e4m3 bytes for an LL_FP8 cache."""
+        return round_e4m3(v).view(torch.uint8) if self.value_fp8 else v.cpu()
+
     def attend(self, layer, q, k, v, commit, rows=None, check=True, what=""):
         """q, k, v: CUDA tensors.  Returns the GPU output (and checks it unless check=False)."""
         out = torch.empty(q.shape, dtype=self.cache.out_dtype, device=q.device)
         self.ll.ll_attend_chunk(self.cache, layer, q, k, v, out, commit)
         if check:
-            qh, kh, vh = self.qk64(q), self.qk64(k), f64(v)
+            qh, kh, vh = self.qk64(q), self.qk64(k), self.v64(v)
             want = self.orc.attend(layer, qh, kh, vh, commit, rows=rows)
             got = out if rows is None else out[torch.as_tensor(rows, device=out.device)]
             compare(got, want, what or "attend", atol=self.atol)
         elif commit:
-            kh, vh = self.qk64(k), f64(v)
+            kh, vh = self.qk64(k), self.v64(v)
             self.orc.commit(layer, kh, vh)
         if commit and self.keep:
             t0 = self.orc.state(layer)[0] - self.C
-            kc, vc = self.key_store(k), v.cpu()
+            kc, vc = self.key_store(k), self.value_store(v)
             for i in range(self.C):
                 self.host[layer][t0 + i] = (kc[i * self.T:(i + 1) * self.T], vc[i * self.T:(i + 1) * self.T])
         return out
@@ -171,25 +183,25 @@ class Lockstep:
 
     def recache(self, layer, k_win, v_win):
         self.ll.ll_recache(self.cache, layer, k_win, v_win)
-        self.orc.recache(layer, self.qk64(k_win), f64(v_win))
+        self.orc.recache(layer, self.qk64(k_win), self.v64(v_win))
         self._keep_recache(layer, k_win, v_win)
 
     def recache_attend(self, layer, q_win, k_win, v_win, rows=None, check=True, what=""):
         out = torch.empty(q_win.shape, dtype=self.cache.out_dtype, device=q_win.device)
         self.ll.ll_recache_attend(self.cache, layer, q_win, k_win, v_win, out)
         if check:
-            want = self.orc.recache_attend(layer, self.qk64(q_win), self.qk64(k_win), f64(v_win), rows=rows)
+            want = self.orc.recache_attend(layer, self.qk64(q_win), self.qk64(k_win), self.v64(v_win), rows=rows)
             got = out if rows is None else out[torch.as_tensor(rows, device=out.device)]
             compare(got, want, what or "recache prefill", atol=self.atol)
         else:
-            self.orc.recache(layer, self.qk64(k_win), f64(v_win))
+            self.orc.recache(layer, self.qk64(k_win), self.v64(v_win))
         self._keep_recache(layer, k_win, v_win)
         return out
 
     def _keep_recache(self, layer, k_win, v_win):
         if not self.keep:
             return
-        kc, vc = self.key_store(k_win), v_win.cpu()
+        kc, vc = self.key_store(k_win), self.value_store(v_win)
         for i, f in enumerate(self.orc.recache_frames(layer)):
             self.host[layer][f] = (kc[i * self.T:(i + 1) * self.T], vc[i * self.T:(i + 1) * self.T])
 

@@ -36,9 +36,10 @@ def ll():
     return mod
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "k8", "fp32", "fp32-d64"])
+@pytest.mark.parametrize("dtype", ["bf16", "k8", "fp8", "fp32", "fp32-d64"])
 def test_allocation_failures_leave_nothing_behind(ll, dtype):
-    code = {"bf16": ll.LL_BF16, "k8": ll.LL_BF16_K8, "fp32": ll.LL_FP32, "fp32-d64": ll.LL_FP32}[dtype]
+    code = {"bf16": ll.LL_BF16, "k8": ll.LL_BF16_K8, "fp8": ll.LL_FP8, "fp32": ll.LL_FP32,
+            "fp32-d64": ll.LL_FP32}[dtype]
     shape = (2, 4, 64 if dtype == "fp32-d64" else 128, 64, 3, 6, 3)
     torch.cuda.synchronize()
     free0 = torch.cuda.mem_get_info()[0]
@@ -57,9 +58,9 @@ def test_allocation_failures_leave_nothing_behind(ll, dtype):
         ll.ll_debug_inject_fault(ll.LL_FAULT_ALLOC, 0)
         cache.close()
         break
-    # bf16: K, V, split scratch, mapped error word; e4m3 keys add the rounding staging; fp32 at
-    # head_dim 128 (CUDA-core kernel) has no scratch, at head_dim 64 (tensor cores) it has
-    assert failures == {"bf16": 4, "k8": 5, "fp32": 3, "fp32-d64": 4}[dtype]
+    # bf16: K, V, split scratch, mapped error word; the e4m3 caches add the rounding staging;
+    # fp32 at head_dim 128 (CUDA-core kernel) has no scratch, at head_dim 64 (tensor cores) it has
+    assert failures == {"bf16": 4, "k8": 5, "fp8": 5, "fp32": 3, "fp32-d64": 4}[dtype]
     torch.cuda.synchronize()
     assert torch.cuda.mem_get_info()[0] == free0
 
@@ -75,10 +76,10 @@ def test_allocation_failure_from_the_environment(ll):
     assert out.stdout.strip() == "status %d" % ll.LL_ERR_OOM, out.stdout
 
 
-@pytest.mark.parametrize("key_fp8", [False, True])
+@pytest.mark.parametrize("key_fp8", ["bf16", "keys", "kv"])
 def test_launch_failures_leave_the_cache_as_it_was(ll, key_fp8):
     H, D, T, S, W, C = 2, 128, 48, 3, 6, 3
-    st = Lockstep(ll, 1, H, D, T, S, W, C, torch.bfloat16, key_fp8=key_fp8)
+    st = Lockstep(ll, 1, H, D, T, S, W, C, torch.bfloat16, key_fp8=(key_fp8 == "keys"), value_fp8=(key_fp8 == "kv"))
     L = C * T
 
     def chunk(tag):

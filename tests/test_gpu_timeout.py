@@ -29,18 +29,20 @@ def ll():
     return mod
 
 
-@pytest.mark.parametrize("T,pair,fp32", [(16, False, False), (1040, False, False), (1040, True, False),
-                                         (16, False, True), (1040, False, True)],
+@pytest.mark.parametrize("T,pair,kind", [(16, False, "bf16"), (1040, False, "bf16"), (1040, True, "bf16"),
+                                         (16, False, "fp32"), (1040, False, "fp32"), (1040, False, "fp8")],
                          ids=["one-cta-small", "one-cta-persistent", "cta-pair-persistent", "tf32-small",
-                              "tf32-persistent"])
-def test_stalled_wait_times_out_and_the_cache_keeps_working(ll, T, pair, fp32):
+                              "tf32-persistent", "fp8-persistent"])
+def test_stalled_wait_times_out_and_the_cache_keeps_working(ll, T, pair, kind):
     """T = 16: one CTA per head pair; T = 1040: a persistent grid with split items, on the
     one-CTA kernel and on the CTA-pair kernel (whose two CTAs must both give up and meet
-    before they free tensor memory), and on the one-CTA kernel with fp32 operands (tf32,
-    head_dim 64), whose V-transpose warps wait as well."""
+    before they free tensor memory), on the one-CTA kernel with fp32 operands (tf32,
+    head_dim 64), whose K-split / V-transpose warps wait as well, and with e4m3 keys and
+    values, whose V-widening warps wait."""
+    fp32 = kind == "fp32"
     H, D, S, W, C = (2, 64, 3, 6, 3) if T == 16 else (12, 64 if fp32 else 128, 3, 6, 3)
     dtype = torch.float32 if fp32 else torch.bfloat16
-    st = Lockstep(ll, 1, H, D, T, S, W, C, dtype)
+    st = Lockstep(ll, 1, H, D, T, S, W, C, dtype, value_fp8=(kind == "fp8"))
     ll.ll_debug_pair_kernel(st.cache, pair)
     L = C * T
     for c in range(3):

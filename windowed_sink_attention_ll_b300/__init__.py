@@ -25,7 +25,7 @@ import torch
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libll.so")
 
-LL_BF16, LL_FP32, LL_BF16_K8 = 0, 1, 2
+LL_BF16, LL_FP32, LL_BF16_K8, LL_FP8 = 0, 1, 2, 3
 STATUS = ["LL_OK", "LL_ERR_INVALID_ARG", "LL_ERR_UNSUPPORTED", "LL_ERR_OOM", "LL_ERR_STATE",
           "LL_ERR_CUDA", "LL_ERR_DEVICE_TIMEOUT"]
 (LL_OK, LL_ERR_INVALID_ARG, LL_ERR_UNSUPPORTED, LL_ERR_OOM, LL_ERR_STATE, LL_ERR_CUDA,
@@ -118,7 +118,9 @@ class LLCache:
         self.T, self.S, self.W, self.C = tokens_per_frame, sink_frames, window_frames, chunk_frames
         self.dtype = dtype
         self.torch_dtype = torch.float32 if dtype == LL_FP32 else torch.bfloat16  # token tensors
-        self.k_cache_dtype = torch.uint8 if dtype == LL_BF16_K8 else self.torch_dtype  # raw K cache (e4m3 bytes)
+        # raw K and V caches (e4m3 caches: their bytes)
+        self.k_cache_dtype = torch.uint8 if dtype in (LL_BF16_K8, LL_FP8) else self.torch_dtype
+        self.v_cache_dtype = torch.uint8 if dtype == LL_FP8 else self.torch_dtype
         self.out_dtype = self.torch_dtype
         self.device = torch.cuda.current_device() if torch.cuda.is_available() else None
 
@@ -253,10 +255,10 @@ def ll_cache_state(cache: LLCache, layer: int):
 
 def ll_cache_read(cache: LLCache, layer: int):
     """Raw K and V of one layer as CPU tensors [H, S+W, T, d] (synchronises); an
-    LL_BF16_K8 cache's K comes back as its e4m3 bytes (torch.uint8)."""
+    LL_BF16_K8 cache's K (an LL_FP8 cache's K and V) comes back as e4m3 bytes (torch.uint8)."""
     shape = (cache.heads, cache.slots, cache.T, cache.head_dim)
     hk = torch.empty(shape, dtype=cache.k_cache_dtype)
-    hv = torch.empty(shape, dtype=cache.torch_dtype)
+    hv = torch.empty(shape, dtype=cache.v_cache_dtype)
     _check(_lib().ll_cache_read(cache.ptr, layer, hk.data_ptr(), hv.data_ptr()), "ll_cache_read")
     return hk, hv
 

@@ -33,10 +33,11 @@
 //               P V product from two blocks of four (one per key half), with
 //               every descriptor ready in registers
 //   warps 4-7   softmax for Q tile 0, warps 8-11 for Q tile 1: thread = row
-//   warps 2-3   fp32 operands only: split each K tile into its tf32 part
-//               and the tf32 rounding of the remainder, and transpose each V
-//               tile into the K-major layout that P V reads (tf32 operands
-//               are taken K-major here); idle otherwise
+//   warps 2-3   fp32 operands: split each K tile into its tf32 part and the
+//               tf32 rounding of the remainder, and transpose each V tile
+//               into the K-major layout that P V reads (tf32 operands are
+//               taken K-major here); e4m3 values: widen each V tile to fp16
+//               (exact) for P V; idle otherwise
 // Tensor memory (512 columns x 128 lanes): O0 [0,128) O1 [128,256)
 // S0 [256,384) S1 [384,512).  P (bf16) overwrites the first 64 columns of S
 // (fp32 operands: P rounded to tf32 overwrites all 128) and feeds the P V
@@ -49,6 +50,9 @@
 // the unused columns [64,128) of their tile's O region, read by the MMA as A);
 // warps 2-3 split each K tile (hi in place, lo into a separate buffer).  P V
 // reads V rounded to tf32 and P rounded to tf32.
+// e4m3 keys and values: Q K^T on kind::f8f6f4; V tiles arrive as e4m3 bytes
+// and are widened to fp16 into one of two buffers; P is packed to fp16 and
+// P V runs on kind::f16 with fp16 A and B.
 // MMA order per key tile j: PV0(j) QK0(j+1) PV1(j) QK1(j+1), so the softmax of
 // one tile overlaps the tensor-core work of the other.  P of a tile is handed
 // over in two halves: once the P of keys 0-63 is in tensor memory the softmax
@@ -81,13 +85,15 @@ constexpr int kThreads = 384;
 static_assert(NQ * BM == kItemRows, "a CTA takes one work item");
 
 // Operand kinds: bf16 Q, K, V (kind::f16); e4m3 Q and K with bf16 V (Q K^T on
-// kind::f8f6f4); fp32 Q, K, V read by the tensor core as tf32 (kind::tf32).
-enum Kind : int { kBf16 = 0, kE4m3 = 1, kTf32 = 2 };
+// kind::f8f6f4); fp32 Q, K, V read by the tensor core as tf32 (kind::tf32);
+// e4m3 Q, K and V (Q K^T on kind::f8f6f4, P V on kind::f16 with fp16 P and V).
+enum Kind : int { kBf16 = 0, kE4m3 = 1, kTf32 = 2, kE4m3KV = 3 };
 
 template <int D, int KIND>
 struct Cfg {
-  static constexpr int kQKElem = KIND == kE4m3 ? 1 : KIND == kTf32 ? 4 : 2;  // bytes per Q / K element
-  static constexpr int kVElem = KIND == kTf32 ? 4 : 2;                        // bytes per V element
+  static constexpr bool kQK8 = KIND == kE4m3 || KIND == kE4m3KV;              // Q K^T on kind::f8f6f4
+  static constexpr int kQKElem = kQK8 ? 1 : KIND == kTf32 ? 4 : 2;            // bytes per Q / K element
+  static constexpr int kVElem = KIND == kTf32 ? 4 : KIND == kE4m3KV ? 1 : 2;  // bytes per V element
   static constexpr int kQKChunks = D * kQKElem / 128;       // 128-byte column chunks of Q and K
   static constexpr int kQKBox = 128 / kQKElem;              // elements per such chunk
   static constexpr int kVChunks = D * kVElem / 128;         // 128-byte column chunks of V
@@ -97,15 +103,19 @@ struct Cfg {
   static constexpr int kVBytes = BN * D * kVElem;           // one V tile
   static constexpr int kTileBytes = kVBytes;                // one ring stage (K or V)
   static constexpr int kQBytes = BM * D * kQKElem;          // one Q tile
-  static constexpr int kNS = KIND == kTf32 ? 3 : 5;         // stages of the K/V tile ring
+  static constexpr int kNS = KIND == kTf32 ? 3 : KIND == kE4m3KV ? 8 : 5;  // stages of the K/V tile ring
   static constexpr int kVTBytes = KIND == kTf32 ? kVBytes : 0;  // one V tile transposed (tf32)
   static constexpr int kKLBytes = KIND == kTf32 ? kKBytes : 0;  // low parts of one K tile (tf32)
+  static constexpr int kV16Tile = BN * D * 2;                   // one V tile widened to fp16 (e4m3 V)
+  static constexpr int kV16Bytes = KIND == kE4m3KV ? 2 * kV16Tile : 0;
   static constexpr int kSmemKV = NQ * kQBytes;
   static constexpr int kSmemVT = kSmemKV + kNS * kTileBytes;
   static constexpr int kSmemKL = kSmemVT + kVTBytes;
-  static constexpr int kSmemBar = kSmemKL + kKLBytes;
-  static constexpr int kSmemBytes = kSmemBar + 256 + 1024;  // barriers, then alignment slack
+  static constexpr int kSmemV16 = kSmemKL + kKLBytes;
+  static constexpr int kSmemBar = kSmemV16 + kV16Bytes;
+  static constexpr int kSmemBytes = kSmemBar + 512 + 1024;  // barriers, then alignment slack
   static_assert(KIND != kTf32 || D == 64, "fp32 tiles fit the shared memory at head_dim 64 only");
+  static_assert(!kQK8 || D == 128, "e4m3 Q K^T: one 128-byte chunk per row");
   static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
 };
 
@@ -249,6 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
   const uint32_t sKV = base + Cf::kSmemKV;
   const uint32_t sVT = base + Cf::kSmemVT;  // fp32 operands: the V tile P V reads, K-major
   const uint32_t sKL = base + Cf::kSmemKL;  // fp32 operands: low parts of the K tile
+  const uint32_t sV16 = base + Cf::kSmemV16;  // e4m3 V: two V tiles widened to fp16
   const uint32_t sBar = base + Cf::kSmemBar;
   const uint32_t bQfull = sBar;
   const uint32_t bQempty = sBar + 8;
@@ -264,8 +275,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
   const uint32_t bKsplit = bDrain + 24;   // fp32 operands: K tile split (hi in place, lo in sKL)
   const uint32_t bKLempty = bDrain + 32;  // fp32 operands: Q K^T of both query tiles done with sKL
   const uint32_t bQsplit = bDrain + 40;   // fp32 operands: both Q tiles split
-  constexpr int kBarBytes = 16 + 16 * NS + 16 + 32 + 24 + 40;
-  static_assert(kBarBytes + 8 <= 256, "barrier area");
+  const uint32_t bWfull0 = bDrain + 48;   // e4m3 V: fp16 buffer b (at +8b) filled
+  const uint32_t bWempty0 = bDrain + 64;  // e4m3 V: P V of both query tiles done with buffer b
+  constexpr int kBarBytes = 16 + 16 * NS + 16 + 32 + 24 + 40 + 32;
+  static_assert(kBarBytes + 8 <= 512, "barrier area");
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + Cf::kSmemBar + kBarBytes);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + Cf::kSmemBar + kBarBytes + 4);
 
@@ -293,6 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     mbar_init(bKsplit, 64);
     mbar_init(bKLempty, 1);
     mbar_init(bQsplit, NQ * 128);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bWfull0 + 8 * b, 64);
+      mbar_init(bWempty0 + 8 * b, 1);
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -355,11 +372,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     {
       // ------------------------------ MMA issuer (whole warp) --------------------
       // Q, K both K-major
-      constexpr uint32_t kIdQK = KIND == kE4m3   ? idesc_e4m3(BM, BN)
+      constexpr uint32_t kIdQK = Cf::kQK8        ? idesc_e4m3(BM, BN)
                                  : KIND == kTf32 ? idesc_tf32(BM, BN)
                                                  : idesc_bf16(BM, BN, 0, 0);
       // P from TMEM; V is N(=d)-major, or K-major after the transpose (tf32)
-      constexpr uint32_t kIdPV = KIND == kTf32 ? idesc_tf32(BM, D) : idesc_bf16(BM, D, 0, 1);
+      constexpr uint32_t kIdPV = KIND == kTf32     ? idesc_tf32(BM, D)
+                                 : KIND == kE4m3KV ? idesc_f16(BM, D, 0, 1)
+                                                   : idesc_bf16(BM, D, 0, 1);
       // The tensor core takes one 128x128x16 MMA per 64 clocks, but this warp
       // shares its SMSP's issue slots with two busy softmax warps and gets few of
       // them, so each MMA group must cost it as few instructions as possible.
@@ -383,7 +402,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         for (int ks = 0; ks < KS; ++ks)
           dq[w][ks] = sw128_desc(sQ + w * Cf::kQBytes + (ks >> 2) * kAtom + (ks & 3) * 32, 16, 1024);
       const uint64_t dK0 = sw128_desc(sKV, 16, 1024);
-      const uint64_t dV0 = sw128_desc(sKV, kAtom, 1024);
+      // V tiles: in the ring, or (e4m3 V) in the two fp16 buffers
+      const uint64_t dV0 = sw128_desc(KIND == kE4m3KV ? sV16 : sKV, kAtom, 1024);
+      constexpr uint32_t kVStride = KIND == kE4m3KV ? Cf::kV16Tile : Cf::kTileBytes;
       const uint32_t k_lo0 = (uint32_t)dK0, k_hi = (uint32_t)(dK0 >> 32);
       const uint32_t v_lo0 = (uint32_t)dV0, v_hi = (uint32_t)(dV0 >> 32);
       // tf32: the transposed V tile sits at one address; k-step ks (8 keys, 32
@@ -403,7 +424,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         uint64_t bd[KS];
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) bd[ks] = make_desc(lo + ((ks >> 2) * kAtom + (ks & 3) * 32) / 16, k_hi);
-        if constexpr (KIND == kE4m3)
+        if constexpr (Cf::kQK8)
           mma4_ss_f8(tmem + 256 + 128 * w, dq[w], bd, kIdQK);
         else if constexpr (KIND == kTf32) {
           const uint32_t sd = tmem + 256 + 128 * w;
@@ -416,7 +437,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         else
           mma4_ss(tmem + 256 + 128 * w, dq[w], bd, kIdQK, 0u);
       };
-      // P V in two groups of k-steps: keys 0-63, then keys 64-127
+      // P V in two groups of k-steps: keys 0-63, then keys 64-127; `stage` is the
+      // ring stage of the V tile (e4m3 V: its fp16 buffer)
       auto issue_pv = [&](int w, int stage, int half, bool acc) {
         if constexpr (KIND == kTf32) {
           uint64_t bd[8];
@@ -424,7 +446,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
           for (int ks = 0; ks < 8; ++ks) bd[ks] = half ? dvt1[ks] : dvt0[ks];
           mma8_ts_tf32(tmem + 128 * w, tmem + 256 + 128 * w + 64 * half, bd, kIdPV, acc ? 1u : 0u);
         } else {
-          const uint32_t lo = v_lo0 + (((uint32_t)stage * Cf::kTileBytes) >> 4);
+          const uint32_t lo = v_lo0 + (((uint32_t)stage * kVStride) >> 4);
           uint64_t bd[4];
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) bd[ks] = make_desc(lo + ((half * 4 + ks) * 16 * 128) / 16, v_hi);
@@ -461,13 +483,18 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
           if constexpr (KIND == kTf32) {
             if (!(ok = __all_sync(0xffffffffu, wait(bVTfull, (jt + t) & 1, ctl)))) break;
           }
+          // e4m3 V: the fp16 buffer of V tile jt + t
+          const int pvs = KIND == kE4m3KV ? ((jt + t) & 1) : sv;
+          if constexpr (KIND == kE4m3KV) {
+            if (!(ok = __all_sync(0xffffffffu, wait(bWfull0 + 8 * pvs, ((jt + t) >> 1) & 1, ctl)))) break;
+          }
           // the previous item's epilogue must have read O out of tensor memory
           if (t == 0 && qi > 0 && !(ok = __all_sync(0xffffffffu, wait(bOempty, (qi - 1) & 1, ctl)))) break;
           tc_fence_after();
-          issue_pv(0, sv, 0, t > 0);
+          issue_pv(0, pvs, 0, t > 0);
           if (!(ok = __all_sync(0xffffffffu, wait(bP0 + 16, (jt + t) & 1, ctl)))) break;
           tc_fence_after();
-          issue_pv(0, sv, 1, true);
+          issue_pv(0, pvs, 1, true);
           if (more) {
             if (!(ok = __all_sync(0xffffffffu, wait(bKVfull0 + 8 * sk, (uk / NS) & 1, ctl)))) break;
             if constexpr (KIND == kTf32) {
@@ -479,12 +506,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
           }
           if (!(ok = __all_sync(0xffffffffu, wait(bP0 + 8, (jt + t) & 1, ctl)))) break;
           tc_fence_after();
-          issue_pv(1, sv, 0, t > 0);
+          issue_pv(1, pvs, 0, t > 0);
           if (!(ok = __all_sync(0xffffffffu, wait(bP0 + 24, (jt + t) & 1, ctl)))) break;
           tc_fence_after();
-          issue_pv(1, sv, 1, true);
+          issue_pv(1, pvs, 1, true);
           tc_commit_e(bKVempty0 + 8 * sv);
           if constexpr (KIND == kTf32) tc_commit_e(bVTempty);
+          if constexpr (KIND == kE4m3KV) tc_commit_e(bWempty0 + 8 * pvs);
           if (more) {
             issue_qk(1, sk);
             tc_commit_e(bS0 + 8);
@@ -567,6 +595,55 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           mbar_arrive(bVTfull);
+        }
+        if (!ok) break;
+        u += 2 * n;
+      }
+    } else if constexpr (KIND == kE4m3KV) {
+      // ------------------------------ V widening (e4m3 values) ---------------------
+      // TMA leaves a V tile as 128 key rows of 128 e4m3 bytes (one column chunk),
+      // 16-byte units swizzled by key % 8.  P V reads fp16 in the layout of a bf16
+      // V tile: column chunk c (d in [64c, 64c+64)) of 128 key rows of 128 bytes,
+      // 16-byte units swizzled by key % 8.  A source unit (16 values of d) widens
+      // exactly (cvt.rn.f16x2.e4m3x2) into two units of one chunk.  Consecutive
+      // threads take consecutive keys: no bank conflicts on either side.
+      const int tt = threadIdx.x - 64;
+      Walker wk;
+      walker_init(wk, p.a, p.s, blockIdx.x);
+      Piece pc;
+      int u = 0, vt = 0;
+      bool ok = true;
+      while (ok && walker_next(wk, p.a, p.s, pc, blockIdx.x)) {
+        const int n = pc.j1 - pc.j0;
+        for (int t = 0; t < n; ++t, ++vt) {
+          const int uv = u + 2 * t + 1, sv = uv % NS;
+          const int b = vt & 1;
+          if (!(ok = wait(bKVfull0 + 8 * sv, (uv / NS) & 1, ctl))) break;
+          // P V of V tile vt - 2 (both query tiles) is done with buffer b
+          if (vt >= 2 && !(ok = wait(bWempty0 + 8 * b, ((vt >> 1) - 1) & 1, ctl))) break;
+          const uint8_t* raw = gbase + Cf::kSmemKV + sv * Cf::kTileBytes;
+          uint8_t* dst = gbase + Cf::kSmemV16 + b * Cf::kV16Tile;
+#pragma unroll 4
+          for (int x = tt; x < BN * 8; x += 64) {
+            const int k = x % BN, q = x / BN;  // key, 16-value unit of d
+            const uint4 val = *reinterpret_cast<const uint4*>(raw + k * 128 + ((q ^ (k & 7)) << 4));
+            const uint32_t w4[4] = {val.x, val.y, val.z, val.w};
+            uint32_t h[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+                  "cvt.rn.f16x2.e4m3x2 %0, a;\n\tcvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+                  : "=r"(h[2 * i]), "=r"(h[2 * i + 1])
+                  : "r"(w4[i]));
+            }
+            uint8_t* row = dst + (q >> 2) * kAtom + k * 128;
+            const int u0 = (q & 3) * 2;
+            *reinterpret_cast<uint4*>(row + ((u0 ^ (k & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(row + (((u0 + 1) ^ (k & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+          }
+          // generic-proxy writes, read by the tensor core (async proxy)
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive(bWfull0 + 8 * b);
         }
         if (!ok) break;
         u += 2 * n;
@@ -710,8 +787,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
             const int c = g * 32 + 2 * i;
             float x0, x1;
             fma_f32x2(x0, x1, __uint_as_float(r[c]), __uint_as_float(r[c + 1]), sl2x2, nmo2);
-            pk[i] = pack_bf16(ex2(x0), ex2(x1));
-            add_bf16x2(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], pk[i]);
+            if constexpr (KIND == kE4m3KV) {
+              pk[i] = pack_f16(ex2(x0), ex2(x1));
+              add_f16x2(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], pk[i]);
+            } else {
+              pk[i] = pack_bf16(ex2(x0), ex2(x1));
+              add_bf16x2(ls[2 * (i & 3)], ls[2 * (i & 3) + 1], pk[i]);
+            }
           }
           tmem_st16(tS + 16 * g, pk);
           if (g == 1 && !rescale) {
@@ -937,6 +1019,7 @@ int attend_schedule_dump(int Lq, int La, int Lb, int heads, int max_ctas, int mo
 }
 
 cudaError_t launch_attend_bf16_tc(const AttendArgs& a, cudaStream_t stream) {
+  if (a.qk_fp8 && a.v_fp8) return a.head_dim == 128 ? launch_tc<128, kE4m3KV>(a, stream) : cudaErrorInvalidValue;
   if (a.qk_fp8) return a.head_dim == 128 ? launch_tc<128, kE4m3>(a, stream) : cudaErrorInvalidValue;
   if (a.head_dim == 64) return launch_tc<64, kBf16>(a, stream);
   return a.pair ? launch_attend_bf16_pair(a, stream) : launch_tc<128, kBf16>(a, stream);

@@ -101,8 +101,8 @@ __global__ void __launch_bounds__(kThreads) copy_frames_kernel(const __grid_cons
 // consecutive values (two 16-byte loads, one 16-byte store).  Launched as a
 // programmatic dependent: it waits for the kernel before it on the stream.
 struct QuantArgs {
-  const uint4* src[2];
-  uint4* dst[2];
+  const uint4* src[3];
+  uint4* dst[3];
   int64_t groups;  // 16-value groups per tensor
 };
 
@@ -144,17 +144,19 @@ cudaError_t launch_copy_frames(const CopyFramesArgs& a, cudaStream_t stream) {
   return e;
 }
 
-cudaError_t launch_quantize_e4m3(const void* src0, void* dst0, const void* src1, void* dst1, int64_t n,
-                                 cudaStream_t stream) {
+cudaError_t launch_quantize_e4m3(const void* const src[3], void* const dst[3], int64_t n, cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
   if (n % 16 != 0) return cudaErrorInvalidValue;
   QuantArgs q;
-  q.src[0] = static_cast<const uint4*>(src0);
-  q.dst[0] = static_cast<uint4*>(dst0);
-  q.src[1] = static_cast<const uint4*>(src1);
-  q.dst[1] = static_cast<uint4*>(dst1);
+  unsigned tensors = 0;
+  for (int t = 0; t < 3; ++t) {
+    q.src[t] = static_cast<const uint4*>(src[t]);
+    q.dst[t] = static_cast<uint4*>(dst[t]);
+    if (src[t]) tensors = (unsigned)t + 1;
+  }
+  if (tensors == 0) return cudaSuccess;
   q.groups = n / 16;
-  const dim3 grid((unsigned)((q.groups + kThreads - 1) / kThreads), src1 ? 2u : 1u);
+  const dim3 grid((unsigned)((q.groups + kThreads - 1) / kThreads), tensors);
   const cudaError_t e = launch_dependent(quantize_e4m3_kernel, grid, dim3(kThreads), 0, stream, q);
   count_launch();
   return e;

@@ -31,14 +31,16 @@ void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 struct ll_cache {
   int L, H, D, T, S, W, C;
   ll_dtype dtype;
-  int eb;                 // element bytes of the token tensors and of the V cache
-  int keb;                // element bytes of the K cache (1: e4m3 keys, LL_BF16_K8)
+  int eb;                 // element bytes of the token tensors
+  int keb;                // element bytes of the K cache (1: e4m3 keys, LL_BF16_K8 and LL_FP8)
+  int veb;                // element bytes of the V cache (1: e4m3 values, LL_FP8)
   int device;
   size_t layer_elems;     // elements of one layer's K (= V)
   void* k = nullptr;      // [L][H][S+W][T][D]
   void* v = nullptr;
-  uint8_t* q8 = nullptr;  // LL_BF16_K8: q and the chunk's (or recache window's) keys rounded to e4m3
+  uint8_t* q8 = nullptr;  // e4m3 caches: q and the chunk's (or recache window's) keys rounded to e4m3
   uint8_t* k8 = nullptr;
+  uint8_t* v8 = nullptr;  // LL_FP8: the values rounded to e4m3
   std::vector<int64_t> n;               // frames committed per layer
   std::vector<int64_t> fos;             // frame_of_slot, L x (S+W)
   unsigned* err_host = nullptr;         // mapped host word written by kernels
@@ -173,9 +175,10 @@ ll::AttendArgs base_args(ll_cache* c, int layer) {
   std::memset(&a, 0, sizeof(a));
   const size_t off = c->layer_elems * (size_t)layer;
   a.kc = static_cast<const char*>(c->k) + off * c->keb;
-  a.vc = static_cast<const char*>(c->v) + off * c->eb;
+  a.vc = static_cast<const char*>(c->v) + off * c->veb;
   a.cache_head_elems = (int64_t)(c->S + c->W) * c->T * c->D;
-  a.qk_fp8 = c->dtype == LL_BF16_K8 ? 1 : 0;
+  a.qk_fp8 = (c->dtype == LL_BF16_K8 || c->dtype == LL_FP8) ? 1 : 0;
+  a.v_fp8 = c->dtype == LL_FP8 ? 1 : 0;
   a.heads = c->H;
   a.head_dim = c->D;
   a.scale_log2 = (float)(1.4426950408889634 / __builtin_sqrt((double)c->D));
@@ -226,14 +229,19 @@ ll_status launch_attend(ll_cache* c, const ll::AttendArgs& a, cudaStream_t st, i
   if (launch_fault()) return LL_ERR_CUDA;
   ProfileScope prof(c, st, kind);
   cudaError_t e;
-  if (c->dtype == LL_BF16_K8) {
-    // keys in e4m3: the attention reads q and its fresh keys rounded the same way,
-    // from the cache's staging buffers (which a commit copy then reads); every
-    // caller here has as many fresh keys as queries
+  if (c->dtype == LL_BF16_K8 || c->dtype == LL_FP8) {
+    // keys (and with LL_FP8 values) in e4m3: the attention reads q and its fresh
+    // keys (and values) rounded the same way, from the cache's staging buffers
+    // (which a commit copy then reads); every caller here has as many fresh keys
+    // as queries
     ll::AttendArgs a8 = a;
-    e = ll::launch_quantize_e4m3(a.q, c->q8, a.kn, c->k8, (int64_t)a.Lq * c->H * c->D, st);
+    const bool v8 = c->dtype == LL_FP8;
+    const void* src[3] = {a.q, a.kn, v8 ? a.vn : nullptr};
+    void* const dst[3] = {c->q8, c->k8, v8 ? c->v8 : nullptr};
+    e = ll::launch_quantize_e4m3(src, dst, (int64_t)a.Lq * c->H * c->D, st);
     a8.q = c->q8;
     a8.kn = c->k8;
+    if (v8) a8.vn = c->v8;
     if (e == cudaSuccess) e = ll::launch_attend_bf16_tc(a8, st);
   } else if (c->use_simt || (c->dtype == LL_FP32 && c->D != 64)) {
     // the CUDA-core kernel: fp32 at head_dim 128 (two fp32 query tiles and a K/V
@@ -256,14 +264,14 @@ ll_status launch_copy(ll_cache* c, int layer, const void* k, const void* v, cons
   a.src_k = k;
   a.src_v = v;
   a.dst_k = static_cast<char*>(c->k) + off * c->keb;
-  a.dst_v = static_cast<char*>(c->v) + off * c->eb;
+  a.dst_v = static_cast<char*>(c->v) + off * c->veb;
   a.k_elem_bytes = c->keb;
   a.frames = (int)slot_of.size();
   a.tokens_per_frame = c->T;
   a.heads = c->H;
   a.head_dim = c->D;
   a.slots = c->S + c->W;
-  a.elem_bytes = c->eb;
+  a.elem_bytes = c->veb;
   for (size_t i = 0; i < slot_of.size(); ++i) a.slot_of[i] = slot_of[i];
   if (launch_fault()) return LL_ERR_CUDA;
   ProfileScope prof(c, st, LL_KERNEL_COPY);
@@ -282,7 +290,7 @@ ll_status check_layer(const ll_cache* c, int layer) {
 // the device has finished with them.
 ll_status poison_slots(ll_cache* c) {
   if (ll_status s = set_device(c)) return s;
-  const size_t kbytes = c->layer_elems * c->L * c->keb, vbytes = c->layer_elems * c->L * c->eb;
+  const size_t kbytes = c->layer_elems * c->L * c->keb, vbytes = c->layer_elems * c->L * c->veb;
   if (cudaDeviceSynchronize() != cudaSuccess || cudaMemset(c->k, 0xFF, kbytes) != cudaSuccess ||
       cudaMemset(c->v, 0xFF, vbytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
     return LL_ERR_CUDA;
@@ -301,7 +309,7 @@ ll_status poison_resident_gaps(ll_cache* c) {
       for (int h = 0; h < c->H; ++h) {
         const size_t e = c->layer_elems * layer + ((size_t)h * slots + slot) * rows;
         if (cudaMemset(static_cast<char*>(c->k) + e * c->keb, 0xFF, rows * c->keb) != cudaSuccess ||
-            cudaMemset(static_cast<char*>(c->v) + e * c->eb, 0xFF, rows * c->eb) != cudaSuccess)
+            cudaMemset(static_cast<char*>(c->v) + e * c->veb, 0xFF, rows * c->veb) != cudaSuccess)
           return LL_ERR_CUDA;
       }
     }
@@ -352,9 +360,9 @@ ll_status ll_cache_create(ll_cache** out, int layers, int heads, int head_dim, i
   if (layers < 1 || heads < 1 || tokens_per_frame < 1 || chunk_frames < 1 || sink_frames < 0 ||
       window_frames < 0)
     return LL_ERR_INVALID_ARG;
-  if (dtype != LL_BF16 && dtype != LL_FP32 && dtype != LL_BF16_K8) return LL_ERR_INVALID_ARG;
+  if (dtype != LL_BF16 && dtype != LL_FP32 && dtype != LL_BF16_K8 && dtype != LL_FP8) return LL_ERR_INVALID_ARG;
   if (head_dim != 64 && head_dim != 128) return LL_ERR_UNSUPPORTED;
-  if (dtype == LL_BF16_K8 && head_dim != 128) return LL_ERR_UNSUPPORTED;
+  if ((dtype == LL_BF16_K8 || dtype == LL_FP8) && head_dim != 128) return LL_ERR_UNSUPPORTED;
   const int slots = sink_frames + window_frames;
   if (slots > ll::kMaxFrameTable || chunk_frames > ll::kMaxFrameTable) return LL_ERR_UNSUPPORTED;
   // kernel grids: (frames x heads) copy blocks; 32-bit token counts per call
@@ -371,7 +379,8 @@ ll_status ll_cache_create(ll_cache** out, int layers, int heads, int head_dim, i
   c->C = chunk_frames;
   c->dtype = dtype;
   c->eb = dtype == LL_FP32 ? 4 : 2;
-  c->keb = dtype == LL_BF16_K8 ? 1 : c->eb;
+  c->keb = (dtype == LL_BF16_K8 || dtype == LL_FP8) ? 1 : c->eb;
+  c->veb = dtype == LL_FP8 ? 1 : c->eb;
   c->layer_elems = (size_t)heads * slots * tokens_per_frame * head_dim;
   c->n.assign(layers, 0);
   c->fos.assign((size_t)layers * slots, -1);
@@ -381,7 +390,7 @@ ll_status ll_cache_create(ll_cache** out, int layers, int heads, int head_dim, i
   }
   // at least one 256-byte block, so a cache without slots (S = W = 0) still
   // hands the kernels a valid base address
-  size_t kbytes = c->layer_elems * layers * c->keb, vbytes = c->layer_elems * layers * c->eb;
+  size_t kbytes = c->layer_elems * layers * c->keb, vbytes = c->layer_elems * layers * c->veb;
   if (kbytes < 256) kbytes = 256;
   if (vbytes < 256) vbytes = 256;
   auto fail = [&](ll_status st) {
@@ -406,12 +415,15 @@ ll_status ll_cache_create(ll_cache** out, int layers, int heads, int head_dim, i
         cudaSuccess)
       return fail(LL_ERR_OOM);
   }
-  if (dtype == LL_BF16_K8) {
-    // staging for q and the fresh keys rounded to e4m3: a chunk, or a recache window
+  if (dtype == LL_BF16_K8 || dtype == LL_FP8) {
+    // staging for q and the fresh keys (and values) rounded to e4m3: a chunk, or a
+    // recache window
     const int frames = chunk_frames > slots ? chunk_frames : slots;
     const size_t n = (size_t)frames * tokens_per_frame * heads * head_dim;
-    if (dev_alloc(reinterpret_cast<void**>(&c->q8), 2 * n) != cudaSuccess) return fail(LL_ERR_OOM);
+    if (dev_alloc(reinterpret_cast<void**>(&c->q8), (dtype == LL_FP8 ? 3 : 2) * n) != cudaSuccess)
+      return fail(LL_ERR_OOM);
     c->k8 = c->q8 + n;
+    if (dtype == LL_FP8) c->v8 = c->q8 + 2 * n;
   }
   if (host_alloc_mapped(reinterpret_cast<void**>(&c->err_host), 256) != cudaSuccess ||
       cudaHostGetDevicePointer(reinterpret_cast<void**>(&c->err_dev), c->err_host, 0) != cudaSuccess) {
@@ -481,8 +493,9 @@ ll_status ll_attend_chunk(ll_cache* c, int layer, const void* q, const void* k, 
     const int64_t f = t0 + i;
     if (f < c->S || f >= win_lo) slot_of[i] = ll_frame_slot(c->S, c->W, f);
   }
-  // an e4m3 key cache takes the keys the attention just rounded
-  if (ll_status s = launch_copy(c, layer, c->dtype == LL_BF16_K8 ? c->k8 : k, v, slot_of, st)) return s;
+  // an e4m3 cache takes the keys (and values) the attention just rounded
+  const bool k8 = c->dtype == LL_BF16_K8 || c->dtype == LL_FP8;
+  if (ll_status s = launch_copy(c, layer, k8 ? c->k8 : k, c->dtype == LL_FP8 ? c->v8 : v, slot_of, st)) return s;
   int64_t* fos = &c->fos[(size_t)layer * (c->S + c->W)];
   for (int i = 0; i < c->C; ++i)
     if (slot_of[i] >= 0) fos[slot_of[i]] = t0 + i;
@@ -526,12 +539,15 @@ static ll_status recache_common(ll_cache* c, int layer, const void* q_win, const
   }
   std::vector<int> slot_of(R);
   for (int i = 0; i < R; ++i) slot_of[i] = ll_frame_slot(c->S, c->W, frames[i]);
-  if (c->dtype == LL_BF16_K8) {
-    // the keys go in rounded to e4m3 (the prefill above already rounded them)
-    if (!q_win && ll::launch_quantize_e4m3(k_win, c->k8, nullptr, nullptr, (int64_t)R * c->T * c->H * c->D, st) !=
-                      cudaSuccess)
+  if (c->dtype == LL_BF16_K8 || c->dtype == LL_FP8) {
+    // the keys (and with LL_FP8 the values) go in rounded to e4m3 (the prefill
+    // above already rounded them)
+    const bool v8 = c->dtype == LL_FP8;
+    const void* src[3] = {nullptr, k_win, v8 ? v_win : nullptr};
+    void* const dst[3] = {nullptr, c->k8, v8 ? c->v8 : nullptr};
+    if (!q_win && ll::launch_quantize_e4m3(src, dst, (int64_t)R * c->T * c->H * c->D, st) != cudaSuccess)
       return LL_ERR_CUDA;
-    return launch_copy(c, layer, c->k8, v_win, slot_of, st);
+    return launch_copy(c, layer, c->k8, v8 ? c->v8 : v_win, slot_of, st);
   }
   return launch_copy(c, layer, k_win, v_win, slot_of, st);
 }
@@ -562,7 +578,7 @@ ll_status ll_set_output_dtype(ll_cache* c, ll_dtype dtype) {
   if (!c) return LL_ERR_INVALID_ARG;
   if (dtype == LL_FP32) {
     c->out_f32 = 1;
-  } else if (dtype == LL_BF16 && (c->dtype == LL_BF16 || c->dtype == LL_BF16_K8)) {
+  } else if (dtype == LL_BF16 && (c->dtype == LL_BF16 || c->dtype == LL_BF16_K8 || c->dtype == LL_FP8)) {
     c->out_f32 = 0;
   } else {
     return LL_ERR_INVALID_ARG;
@@ -612,7 +628,7 @@ ll_status ll_cache_state(ll_cache* c, int layer, int64_t* frames_committed, int6
 ll_status ll_cache_read(ll_cache* c, int layer, void* host_k, void* host_v) {
   NvtxRange range("ll_cache_read");
   if (ll_status s = check_layer(c, layer)) return s;
-  const size_t kbytes = c->layer_elems * c->keb, vbytes = c->layer_elems * c->eb;
+  const size_t kbytes = c->layer_elems * c->keb, vbytes = c->layer_elems * c->veb;
   if (kbytes == 0) return ll_sync(c);  // no slots (S = W = 0): nothing to copy
   if (!host_k || !host_v) return LL_ERR_INVALID_ARG;
   if (ll_status s = ll_sync(c)) return s;

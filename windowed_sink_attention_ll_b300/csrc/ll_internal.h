@@ -34,11 +34,11 @@ struct CopyFramesArgs {
 
 cudaError_t launch_copy_frames(const CopyFramesArgs& a, cudaStream_t stream);
 
-// Round `n` bf16 values of each of two tensors to e4m3 (round to nearest even,
-// saturating at +-448), as the FP8-key cache stores keys and the kind::f8f6f4
-// Q K^T product reads q and the chunk's keys.  src1/dst1 may be null.
-cudaError_t launch_quantize_e4m3(const void* src0, void* dst0, const void* src1, void* dst1, int64_t n,
-                                 cudaStream_t stream);
+// Round `n` bf16 values of each of up to three tensors to e4m3 (round to nearest
+// even, saturating at +-448), as the FP8 caches store keys (and values) and the
+// kind::f8f6f4 Q K^T product reads q and the chunk's keys.  Null entries of src
+// are skipped.
+cudaError_t launch_quantize_e4m3(const void* const src[3], void* const dst[3], int64_t n, cudaStream_t stream);
 
 // ---------------------------------------------------------------------------
 // Attention over two key/value sources:
@@ -76,6 +76,7 @@ struct AttendArgs {
   int scratch_slots;  // partial-result slots the scratch holds
   int pair;           // head_dim 128: the CTA-pair tensor-core kernel instead of the one-CTA kernel
   int qk_fp8;         // q, kn and the cache K hold e4m3 bytes (Q K^T on kind::f8f6f4); head_dim 128
+  int v_fp8;          // with qk_fp8: vn and the cache V hold e4m3 bytes too (P V on fp16 operands)
 };
 
 // bf16 attention on the tensor cores: the one-CTA kernel, or for head_dim 128 with

@@ -185,6 +185,18 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// s0 += low f16 of pk, s1 += high f16 of pk (widened exactly, fp32 adds)
+__device__ __forceinline__ void add_f16x2(float& s0, float& s1, uint32_t pk) {
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\tadd.rn.f32.f16 %0, lo, %0;\n\t"
+      "add.rn.f32.f16 %1, hi, %1;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "r"(pk));
+}
 
 // Shared-memory matrix descriptor, 128-byte swizzle (tcgen05 format: start
 // address, leading and stride byte offsets in 16-byte units, version 1).
@@ -206,6 +218,11 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
 // both operands K-major.
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
   return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+// Instruction descriptor, kind::f16: f16 A and B (format code 0), fp32 D, M x N, A/B major-ness.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
 }
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M x N, A/B major-ness.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_mn) {
