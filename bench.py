@@ -111,9 +111,15 @@ def set_options(ll, cache, args):
         ll.ll_debug_pair_kernel(cache, True)
 
 
-def append_bytes(shape: llsynth.Shape, frames_written: int):
-    """K and V: read from the chunk tensors and written to the cache, per committed frame."""
-    return 2 * 2 * frames_written * shape.tokens_per_frame * shape.heads * shape.head_dim * 2
+def append_bytes(shape: llsynth.Shape, frames_written: int, kv_elem_bytes: int = 4):
+    """K and V: read from the chunk tensors (or the e4m3 staging) and written to the cache,
+    per committed frame.  kv_elem_bytes: bytes of one K element plus one V element in the
+    cache (4 in bf16, 3 with e4m3 keys, 2 with e4m3 keys and values)."""
+    return 2 * frames_written * shape.tokens_per_frame * shape.heads * shape.head_dim * kv_elem_bytes
+
+
+def kv_elem_bytes(args):
+    return 2 if args.kv_fp8 else 3 if args.key_fp8 else 4
 
 
 def frames_written(shape: llsynth.Shape, t0: int):
@@ -475,7 +481,8 @@ def run_ours(args, world, rank, local):
     n_cp, ms_cp = prof[ll.LL_KERNEL_COPY]
     # the bracketed launches are one in ten of each kind: layers 0, 10, 20 of every chunk
     att_sampled = sum(pair_flops(chunk_pairs(shape, t0, args.chunk_mask), H, d) * 3 for t0, _ in plan) * args.steps
-    cp_sampled = sum(append_bytes(shape, frames_written(shape, t0)) * 3 for t0, _ in plan) * args.steps
+    cp_sampled = sum(append_bytes(shape, frames_written(shape, t0), kv_elem_bytes(args)) * 3
+                     for t0, _ in plan) * args.steps
     pk, pk_src = peaks()
     config = {"workload": "stream30: 30 layers x 20 chunks (60 latent frames), H=12, d=128, "
                           "T=1560, C=3, S=3, W=9, 1 committed pass per chunk"}
@@ -647,7 +654,8 @@ def run_single(args, world, rank, local):
     result.update({
         "tflops": pass_flops * passes * args.steps * world / (ms_max / 1e3) / 1e12,
         "roofline": roof,
-        "append": hbm_roofline("copy_frames_kernel", append_bytes(shape, C) * args.steps, n_cp, ms_cp, pk),
+        "append": hbm_roofline("copy_frames_kernel", append_bytes(shape, C, kv_elem_bytes(args)) * args.steps,
+                               n_cp, ms_cp, pk),
         "gpu_launches": launches, "clocks": clocks,
     })
     cache.close()
