@@ -455,11 +455,15 @@ def run_ours(args, world, rank, local):
     L = C * T
     plan = stream_plan(shape, chunks)
     step_frames = chunks * C
-    step_flops = sum(pair_flops(chunk_pairs(shape, t0, args.chunk_mask), H, d) for t0, _ in plan) * shape.layers
+    P = args.passes  # query passes per chunk through all layers; the last one commits
+    step_flops = sum(pair_flops(chunk_pairs(shape, t0, args.chunk_mask), H, d) for t0, _ in plan) * shape.layers * P
 
-    # inputs: independent seeded q/k/v per (rank, layer, chunk), resident before timing
+    # inputs: independent seeded q/k/v per (rank, layer, chunk), resident before timing; with
+    # several passes, the earlier (non-committing) passes get their own q/k/v too
     inputs = [[tuple(llsynth.seeded_normal(("bench", rank, l, c, t), (L, H, d), device="cuda") for t in "qkv")
                for c in range(chunks)] for l in range(shape.layers)]
+    early = [[[tuple(llsynth.seeded_normal(("bench-pass", rank, l, c, p, t), (L, H, d), device="cuda") for t in "qkv")
+               for p in range(P - 1)] for c in range(chunks)] for l in range(shape.layers)]
     outs = [torch.empty((L, H, d), dtype=torch.bfloat16, device="cuda") for _ in range(shape.layers)]
     cache = ll.ll_cache_create(shape.layers, H, d, T, S, W, C, cache_dtype(ll, args))
     set_options(ll, cache, args)
@@ -469,6 +473,11 @@ def run_ours(args, world, rank, local):
         ll.ll_reset(cache)
         st = torch.cuda.current_stream()  # the capture stream while a CUDA graph is recorded
         for c in range(chunks):
+            # as a denoising loop runs the stack: every pass through all layers, the last commits
+            for p in range(P - 1):
+                for l in range(shape.layers):
+                    q, k, v = early[l][c][p]
+                    ll.ll_attend_chunk(cache, l, q, k, v, outs[l], False, st)
             for l in range(shape.layers):
                 q, k, v = inputs[l][c]
                 ll.ll_attend_chunk(cache, l, q, k, v, outs[l], True, st)
@@ -479,17 +488,20 @@ def run_ours(args, world, rank, local):
     ms_max = max_over_ranks(ms, world)
     n_att, ms_att = prof[ll.LL_KERNEL_ATTEND]
     n_cp, ms_cp = prof[ll.LL_KERNEL_COPY]
-    # the bracketed launches are one in ten of each kind: layers 0, 10, 20 of every chunk
-    att_sampled = sum(pair_flops(chunk_pairs(shape, t0, args.chunk_mask), H, d) * 3 for t0, _ in plan) * args.steps
+    # the bracketed launches are one in ten of each kind: layers 0, 10, 20 of every pass of every chunk
+    att_sampled = sum(pair_flops(chunk_pairs(shape, t0, args.chunk_mask), H, d) * 3 * P
+                      for t0, _ in plan) * args.steps
     cp_sampled = sum(append_bytes(shape, frames_written(shape, t0), kv_elem_bytes(args)) * 3
                      for t0, _ in plan) * args.steps
     pk, pk_src = peaks()
     config = {"workload": "stream30: 30 layers x 20 chunks (60 latent frames), H=12, d=128, "
-                          "T=1560, C=3, S=3, W=9, 1 committed pass per chunk"}
+                          "T=1560, C=3, S=3, W=9, %s" % (
+                              "1 committed pass per chunk" if P == 1 else
+                              "%d passes per chunk through all layers (the last commits)" % P)}
     config.update(shape_config(shape, {
-        "chunks": chunks,
+        "chunks": chunks, "passes": P,
         "l2": "inputs larger than L2 (%.1f GB q/k/v + %.2f GB cache per rank)" % (
-            3 * L * H * d * 2 * chunks * shape.layers / 1e9, 2 * shape.layers * (S + W) * T * H * d * 2 / 1e9),
+            3 * L * H * d * 2 * chunks * shape.layers * P / 1e9, 2 * shape.layers * (S + W) * T * H * d * 2 / 1e9),
         "chunk_mask": args.chunk_mask, "recache_scope": args.recache_scope,
         "parallelism": "replicas x%d (independent streams, no collective)" % world}))
     result = base_result(args, world, step_frames * args.steps * world / (ms_max / 1e3), ms_max, config)
@@ -510,10 +522,10 @@ def run_ours(args, world, rank, local):
         "gpu_launches": launches,
         "clocks": clocks,
     })
-    if not args.no_e2e:
+    if not args.no_e2e and P == 1:
         result["e2e"] = run_e2e(ll, cache, shape, chunks, step_frames, world, rank, args)
     cache.close()
-    del inputs
+    del inputs, early
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         rate, threads, sample = oracle_rate(shape)
         result["cpu_baseline"] = {"value": step_frames / (step_flops / rate), "unit": UNIT, "cores": threads,
@@ -586,11 +598,14 @@ def run_graph(args, world, local, ll, cache, step, step_frames, step_flops, shap
     ms, clocks, _, _ = timed_region(args, world, local, [cache], g.replay)
     ms_max = max_over_ranks(ms, world)
     H, d = shape.heads, shape.head_dim
+    P = args.passes
     config = {"workload": "stream30 as one CUDA graph: 30 layers x 20 chunks (60 latent frames), H=12, d=128, "
-                          "T=1560, C=3, S=3, W=9, 1 committed pass per chunk"}
-    config.update(shape_config(shape, {"chunks": chunks, "chunk_mask": args.chunk_mask,
+                          "T=1560, C=3, S=3, W=9, %s" % (
+                              "1 committed pass per chunk" if P == 1 else
+                              "%d passes per chunk through all layers (the last commits)" % P)}
+    config.update(shape_config(shape, {"chunks": chunks, "passes": P, "chunk_mask": args.chunk_mask,
                                        "l2": "inputs larger than L2 (%.1f GB q/k/v)" % (
-                                           3 * L * H * d * 2 * chunks * shape.layers / 1e9),
+                                           3 * L * H * d * 2 * chunks * shape.layers * P / 1e9),
                                        "parallelism": "replicas x%d (independent streams, no collective)" % world}))
     result = base_result(args, world, step_frames * args.steps * world / (ms_max / 1e3), ms_max, config)
     result.update({
@@ -855,7 +870,7 @@ def run_reference(args, world, rank):
     L = C * T
     plan = stream_plan(shape, chunks)
     step_frames = chunks * C
-    step_flops = sum(attend_flops(L, lkv, H, d) for _, lkv in plan) * shape.layers
+    step_flops = sum(attend_flops(L, lkv, H, d) for _, lkv in plan) * shape.layers * args.passes
     budget = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
     if args.ref_budget_s is not None:
         budget = args.ref_budget_s
@@ -873,7 +888,9 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": "stream30: 30 layers x 20 chunks (60 latent frames), H=12, d=128, T=1560, "
-                               "C=3, S=3, W=9 (float64 CPU oracle, sampled rows; step time scaled by flops)"},
+                               "C=3, S=3, W=9, %s (float64 CPU oracle, sampled rows; step time scaled by "
+                               "flops)" % ("1 committed pass per chunk" if args.passes == 1 else
+                                           "%d passes per chunk (the last commits)" % args.passes)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -896,6 +913,9 @@ def main():
                     help="resident (default): recache rewrites sink and window; window: the sink keeps its K/V")
     ap.add_argument("--key-fp8", action="store_true",
                     help="an FP8-key cache (LL_BF16_K8): keys stored in e4m3, Q K^T at the FP8 tensor rate")
+    ap.add_argument("--passes", type=int, default=1,
+                    help="stream30: query passes per chunk through all layers, the last one committing "
+                         "(default 1; e2e is measured at 1 only)")
     ap.add_argument("--kv-fp8", action="store_true",
                     help="an FP8 cache (LL_FP8): keys and values stored in e4m3, Q K^T at the FP8 tensor rate, "
                          "P V on fp16 operands")
