@@ -17,15 +17,17 @@
 // (the frame-causal chunk).
 //
 // This is the one-CTA form of the kernel, the one every bf16 attention runs on
-// (and fp32 attention at head_dim 64, with tf32 operands); ll_attend_pair.cu
-// holds a CTA-pair form for head_dim 128 (selected on request).
+// (as do the e4m3 caches, and fp32 attention at head_dim 64 with tf32
+// operands); ll_attend_pair.cu holds a CTA-pair form for bf16 at head_dim 128
+// (selected on request).
 // Work item = one head x 256 query rows (two 128-row tiles that share every
 // K/V tile); one CTA per SM walks several items (see "Work schedule" in
 // ll_tc_common.cuh):
 // attend launches run whole rounds of items, then split the left-over items
 // into runs of key tiles merged by combine_kernel; prefill launches hand out
 // their unequal items longest first in zigzag rounds.  Warp roles (384 threads):
-//   warp 0      TMA producer: Q per item, then K0 V0 K1 V1 ... into a 5-stage ring
+//   warp 0      TMA producer: Q per item, then K0 V0 K1 V1 ... into a ring of 5
+//               stages (3 with fp32 operands, 8 with e4m3 keys and values)
 //   warp 1      TMEM allocator and MMA issuer: the whole warp runs the issue
 //               loop in step (every wait is a warp vote), and one lane chosen
 //               by elect.sync issues each tcgen05.mma and tcgen05.commit; the
@@ -39,9 +41,9 @@
 //               taken K-major here); e4m3 values: widen each V tile to fp16
 //               (exact) for P V; idle otherwise
 // Tensor memory (512 columns x 128 lanes): O0 [0,128) O1 [128,256)
-// S0 [256,384) S1 [384,512).  P (bf16) overwrites the first 64 columns of S
-// (fp32 operands: P rounded to tf32 overwrites all 128) and feeds the P V
-// product straight from tensor memory.
+// S0 [256,384) S1 [384,512).  P (bf16; fp16 with e4m3 values) overwrites the
+// first 64 columns of S (fp32 operands: P rounded to tf32 overwrites all 128)
+// and feeds the P V product straight from tensor memory.
 // fp32 operands (head_dim 64): Q K^T is kept accurate to fp32 by splitting
 // each operand x into hi = tf32(x) and lo = tf32(x - hi) and summing three
 // tf32 products, S = Qhi Khi^T + Qlo Khi^T + Qhi Klo^T (the split-operand
@@ -64,7 +66,8 @@
 // threads may rescale O in place.  The reference max of a row moves only when
 // the running max grows by more than 2^8 (then O and l are rescaled); every
 // P, the row sum l and the final 1/l use that same reference, so the result
-// is unchanged.  The row sum adds the bf16-rounded P that enters P V.
+// is unchanged.  The row sum adds the rounded P (bf16, fp16 or tf32) that
+// enters P V.
 
 // Every mbarrier wait is bounded (globaltimer).  A wait that runs out sets a
 // CTA-wide abort flag and the device error word; all roles then leave their
