@@ -7,7 +7,9 @@ each pass committing) can be recorded with torch.cuda.graph and replayed
 over the rolling sink + window cache).  The replay's outputs and raw cache bytes
 must equal an eager run's bit for bit, and the replayed outputs must match the
 float64 oracle driven through the same calls (sampled query rows, every layer
-and chunk, the usual bound: max |err| <= 1e-2, relative L2 <= 5e-3).
+and chunk, the usual bound: max |err| <= 1e-2, relative L2 <= 5e-3).  The e4m3
+key-and-value cache records its rounding kernel in the graph as well; its oracle
+is fed the rounded q, k and v.
 """
 
 import pytest
@@ -15,7 +17,7 @@ import torch
 
 import llsynth
 import oracle
-from tests.gpu_util import compare, f64, sample_rows
+from tests.gpu_util import compare, f64, round_e4m3, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -32,11 +34,11 @@ def ll():
     return mod
 
 
-@pytest.mark.parametrize("mask", ["chunk", "frame"])
-def test_stream_replayed_from_a_cuda_graph_equals_eager_and_oracle(ll, mask):
+@pytest.mark.parametrize("mask,kind", [("chunk", "bf16"), ("frame", "bf16"), ("chunk", "fp8")])
+def test_stream_replayed_from_a_cuda_graph_equals_eager_and_oracle(ll, mask, kind):
     layers, H, D, T, S, W, C, chunks = 2, 12, 128, 1040, 3, 6, 3, 6  # 156 items: split tail too
     L = C * T
-    cache = ll.ll_cache_create(layers, H, D, T, S, W, C, ll.LL_BF16)
+    cache = ll.ll_cache_create(layers, H, D, T, S, W, C, ll.LL_FP8 if kind == "fp8" else ll.LL_BF16)
     ll.ll_set_chunk_mask(cache, mask)
     inputs = [[tuple(llsynth.seeded_normal(("graph", l, c, t), (L, H, D), device="cuda") for t in "qkv")
                for c in range(chunks)] for l in range(layers)]
@@ -75,10 +77,10 @@ def test_stream_replayed_from_a_cuda_graph_equals_eager_and_oracle(ll, mask):
     rows = sample_rows(L, 96, seed=7)
     for c in range(chunks):
         for l in range(layers):
-            q, k, v = (f64(t) for t in inputs[l][c])
+            q, k, v = (f64(round_e4m3(t)) if kind == "fp8" else f64(t) for t in inputs[l][c])
             want = orc.attend(l, q, k, v, True, rows=rows)
             compare(outs[l][c][torch.as_tensor(rows, device="cuda")], want,
-                    "graph replay vs oracle, mask %s, layer %d chunk %d" % (mask, l, c))
+                    "graph replay vs oracle, %s cache, mask %s, layer %d chunk %d" % (kind, mask, l, c))
     for l in range(layers):
         assert ll.ll_cache_state(cache, l) == orc.state(l), l
     cache.close()
