@@ -1,8 +1,10 @@
 """Random call sequences through the C ABI, in lockstep with the oracle.
 
 Each case draws a shape (ragged tokens per frame, any sink / window / chunk
-sizes including zero sink and zero window), a dtype (fp32: the CUDA-core
-kernel; bf16: the tensor-core kernel) and a sequence of calls: committing and
+sizes including zero sink and zero window), a dtype (bf16: the tensor-core
+kernel; fp32: the tensor-core kernel with tf32 operands at head_dim 64, the
+CUDA-core kernel at 128; a second set of cases uses the e4m3 caches, keys or
+keys and values, at head_dim 128) and a sequence of calls: committing and
 non-committing chunk passes, recache with and without the prefill attention,
 reset, and switches of the two optional readings (chunk mask, recache scope)
 between calls.  After every call the outputs are compared with the float64
@@ -22,6 +24,7 @@ from tests.gpu_util import Lockstep
 pytestmark = pytest.mark.gpu
 
 CASES = 40
+E4M3_CASES = 16
 OPS = ["commit", "commit", "commit", "commit", "pass", "pass", "prefill", "recache", "reset", "options"]
 
 
@@ -56,8 +59,21 @@ def draw_case(seed):
 @pytest.mark.parametrize("seed", range(CASES))
 def test_random_call_sequence(ll, seed):
     rng, s, dtype, ops = draw_case(seed)
+    run_case(ll, seed, rng, s, dtype, ops, None)
+
+
+@pytest.mark.parametrize("seed", range(CASES, CASES + E4M3_CASES))
+def test_random_call_sequence_e4m3_caches(ll, seed):
+    """The same kind of sequences on the e4m3 caches (head_dim 128): even seeds store keys in
+    e4m3, odd seeds keys and values."""
+    rng, s, _, ops = draw_case(seed)
+    s["D"] = 128
+    run_case(ll, seed, rng, s, torch.bfloat16, ops, "keys" if seed % 2 == 0 else "kv")
+
+
+def run_case(ll, seed, rng, s, dtype, ops, e4m3):
     H, D, T, S, W, C = s["H"], s["D"], s["T"], s["S"], s["W"], s["C"]
-    st = Lockstep(ll, s["layers"], H, D, T, S, W, C, dtype)
+    st = Lockstep(ll, s["layers"], H, D, T, S, W, C, dtype, key_fp8=(e4m3 == "keys"), value_fp8=(e4m3 == "kv"))
     mask, scope = "chunk", "resident"
     L = C * T
 
@@ -67,7 +83,7 @@ def test_random_call_sequence(ll, seed):
 
     for i, op in enumerate(ops):
         layer = int(rng.integers(0, s["layers"]))
-        what = "seed %d op %d %s layer %d %s %s/%s" % (seed, i, op, layer, s, mask, scope)
+        what = "seed %d op %d %s layer %d %s %s/%s %s" % (seed, i, op, layer, s, mask, scope, e4m3 or dtype)
         if op in ("commit", "pass"):
             q, k, v = inputs(i, L)
             st.attend(layer, q, k, v, commit=(op == "commit"), what=what)
