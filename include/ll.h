@@ -323,24 +323,10 @@ LL_API ll_status ll_debug_inject_fault(int kind, int n);
  * (*split_ints = ints written).  Returns the number of pieces (-1 on bad
  * arguments: a size below 1, a mode other than 0-2, block_tokens < 1 in
  * modes 1 and 2).  Items are (head, 256-row query block): head-major in mode 0,
- * last query block first in mode 1; key tiles hold 128 keys.  When the last
- * query block of a head has at most 128 rows and there are two heads or more,
- * the last blocks of heads 2i and 2i+1 share one item (its two 128-row query
- * tiles belong to the two heads): after all other items in modes 0 and 2,
- * before them in mode 1.  This is the schedule of the bf16 and e4m3-key
- * kernels; ll_debug_tile_geom gives each item's tiles.
+ * last query block first in mode 1; key tiles hold 128 keys.
  */
 LL_API int ll_debug_attend_schedule(int Lq, int La, int Lb, int heads, int max_ctas, int mode, int block_tokens,
                                     int* grid, int* pieces, int cap, int* splits, int split_cap, int* split_ints);
-
-/*
- * Test hook (host only): the head and first query row of query tile `tile`
- * (0 or 1; 128 rows each) of work item `item` in the schedule above.  Returns
- * the launch's item count, or -1 on bad arguments (Lq, heads < 1; tile not 0 or
- * 1; item out of range; NULL outputs).  A tile whose first row is at or past Lq
- * holds no query.
- */
-LL_API int ll_debug_tile_geom(int Lq, int heads, int mode, int item, int tile, int* head, int* q0);
 
 /*
  * ll_attend_chunk_noalloc -- the attention of ll_attend_chunk (no commit) for

@@ -1,44 +1,11 @@
 """CPU checks of the tensor-core attend kernel's work schedule, replayed on the host by
-the library itself (ll_debug_attend_schedule runs the same walker the kernel runs, and
-ll_debug_tile_geom the same item geometry).
-
-Items are one head x 256 query rows (two 128-row query tiles); when a head's last query
-block has at most 128 rows, the last blocks of two heads share one item, one query tile
-each.  Every (head, query row) must belong to exactly one tile of one item, and every
-(item, key tile) to exactly one piece of work.
-"""
+the library itself (ll_debug_attend_schedule runs the same walker the kernel runs)."""
 
 import collections
 
 import pytest
 
 from windowed_sink_attention_ll_b300 import build_lib
-
-
-def item_tiles(ll, Lq, H, mode):
-    """[(head, q0) of tile 0, (head, q0) of tile 1] per item, from the library."""
-    n = ll.ll_debug_tile_geom(Lq, H, mode, 0, 0)[2]
-    return [[ll.ll_debug_tile_geom(Lq, H, mode, i, w)[:2] for w in (0, 1)] for i in range(n)]
-
-
-def check_rows_covered_once(tiles, Lq, H):
-    """Every query row of every head in exactly one tile; no tile inside past the rows."""
-    seen = collections.Counter()
-    for item in tiles:
-        for head, q0 in item:
-            assert 0 <= head < H and q0 >= 0 and q0 % 128 == 0
-            for r in range(q0, min(q0 + 128, Lq)):
-                seen[(head, r)] += 1
-    assert len(seen) == Lq * H and set(seen.values()) == {1}
-
-
-def expected_items(Lq, H):
-    """The item count the sharing rule gives (the rule, restated)."""
-    nqb = -(-Lq // 256)
-    last = Lq - (nqb - 1) * 256
-    if H >= 2 and last <= 128:
-        return H * (nqb - 1) + (H + 1) // 2
-    return H * nqb
 
 SHAPES = [
     # Lq,   La,    Lb,  heads, max_ctas
@@ -67,10 +34,8 @@ def ll():
 def test_schedule_covers_every_key_tile_once(ll, shape):
     Lq, La, Lb, H, max_ctas = shape
     grid, pieces, splits = ll.ll_debug_attend_schedule(Lq, La, Lb, H, max_ctas)
-    tiles = item_tiles(ll, Lq, H, 0)
-    items = len(tiles)
-    assert items == expected_items(Lq, H)
-    check_rows_covered_once(tiles, Lq, H)
+    nqb = -(-Lq // 256)
+    items = nqb * H
     nkv = -(-La // 128) + -(-Lb // 128)
     assert 1 <= grid <= min(max_ctas, items)
     seen = collections.Counter()
@@ -105,27 +70,10 @@ def test_schedule_covers_every_key_tile_once(ll, shape):
 def test_schedule_splits_only_leftover_items(ll):
     grid, pieces, splits = ll.ll_debug_attend_schedule(4680, 18720, 4680, 12, 148)
     assert grid == 148
-    # 4680 rows = 18 blocks of 256 + 72: the 12 heads' short last blocks share 6 items, so
-    # 12 x 18 + 6 = 222 items: round 0 = items 0..147 whole, items 148..221 split
-    tiles = item_tiles(ll, 4680, 12, 0)
-    assert len(tiles) == 222
-    assert all(t[0][0] == t[1][0] for t in tiles[:216])                # one head each
-    assert [(t[0][0], t[1][0]) for t in tiles[216:]] == [(2 * i, 2 * i + 1) for i in range(6)]
-    assert all(t[0][1] == t[1][1] == 18 * 256 for t in tiles[216:])   # same rows, two heads
+    # 228 items: round 0 = items 0..147 whole, items 148..227 shared by all 148 CTAs
     whole = {p[1] for p in pieces if not p[4]}
     assert set(range(148)) <= whole
     assert all(item >= 148 for item, _ in splits)
-
-
-def test_odd_head_count_leaves_the_last_short_block_alone(ll):
-    tiles = item_tiles(ll, 300, 3, 0)   # 300 rows = 256 + 44 per head
-    assert len(tiles) == 3 + 2
-    assert tiles[3] == [(0, 256), (1, 256)]
-    assert tiles[4] == [(2, 256), (2, 384)]  # its second tile lies past the last row
-    check_rows_covered_once(tiles, 300, 3)
-    # one head, or a last block of more than 128 rows: no sharing
-    assert len(item_tiles(ll, 300, 1, 0)) == 2
-    assert len(item_tiles(ll, 400, 4, 0)) == 8
 
 
 PREFILL = [
@@ -142,25 +90,20 @@ PREFILL = [
 def test_prefill_schedule_covers_every_item_once_and_balances(ll, shape):
     Lq, La, block, H, max_ctas = shape
     grid, pieces, splits = ll.ll_debug_attend_schedule(Lq, La, Lq, H, max_ctas, mode=1, block_tokens=block)
-    tiles = item_tiles(ll, Lq, H, 1)
-    items = len(tiles)
-    assert items == expected_items(Lq, H)
-    check_rows_covered_once(tiles, Lq, H)
+    nqb = -(-Lq // 256)
+    items = nqb * H
     assert grid == min(max_ctas, items) and splits == []
     seen = collections.Counter()
     load = collections.Counter()
     for cta, item, j0, j1, partial, slot in pieces:
         assert 0 <= cta < grid and 0 <= item < items and j0 == 0 and partial == 0
-        qb = tiles[item][0][1] // 256                   # last query block first
+        qb = nqb - 1 - item // H                       # last query block first
         last_row = min(Lq, (qb + 1) * 256) - 1
         kv_end = min(Lq, (last_row // block + 1) * block)
         assert j1 == -(-La // 128) + -(-kv_end // 128)  # every cached tile + the fresh tiles it may see
         seen[item] += 1
         load[cta] += j1
     assert len(seen) == items and set(seen.values()) == {1}
-    # longest first: the query blocks never grow along the item numbers
-    qbs = [t[0][1] // 256 for t in tiles]
-    assert qbs == sorted(qbs, reverse=True)
     # zigzag rounds over items sorted longest first: no CTA carries much more than the mean
     if items > grid:
         mean = sum(load.values()) / grid
@@ -169,7 +112,8 @@ def test_prefill_schedule_covers_every_item_once_and_balances(ll, shape):
 
 
 def _check_attend(grid, pieces, splits, Lq, La, Lb, H, max_ctas):
-    items = expected_items(Lq, H)
+    nqb = -(-Lq // 256)
+    items = nqb * H
     nkv = -(-La // 128) + -(-Lb // 128)
     assert grid == min(max_ctas, 256, items)
     seen = collections.Counter()
@@ -219,8 +163,6 @@ def test_random_attend_schedules():
         shape = (Lq, La, Lq, H, max_ctas)
         grid, pieces, splits = ll.ll_debug_attend_schedule(*shape)
         _check_attend(grid, pieces, splits, *shape)
-        if _ < 40:
-            check_rows_covered_once(item_tiles(ll, Lq, H, 0), Lq, H)
         # the frame-causal chunk (mode 2) runs the attend schedule unchanged
         block = int(rng.integers(1, Lq + 1))
         assert ll.ll_debug_attend_schedule(*shape, mode=2, block_tokens=block) == (grid, pieces, splits), shape
@@ -239,17 +181,14 @@ def test_random_prefill_schedules():
         H = int(rng.integers(1, 25))
         max_ctas = int(rng.choice([1, 3, 64, 148, 300]))
         grid, pieces, splits = ll.ll_debug_attend_schedule(Lq, La, Lq, H, max_ctas, mode=1, block_tokens=block)
-        tiles = item_tiles(ll, Lq, H, 1)
-        items = len(tiles)
-        assert items == expected_items(Lq, H)
-        if _ < 40:
-            check_rows_covered_once(tiles, Lq, H)
+        nqb = -(-Lq // 256)
+        items = nqb * H
         assert grid == min(max_ctas, items) and splits == []
         seen = collections.Counter()
         load = collections.Counter()
         for cta, item, j0, j1, partial, slot in pieces:
             assert 0 <= cta < grid and 0 <= item < items and j0 == 0 and partial == 0
-            qb = tiles[item][0][1] // 256
+            qb = nqb - 1 - item // H
             last_row = min(Lq, (qb + 1) * 256) - 1
             kv_end = min(Lq, (last_row // block + 1) * block)
             assert j1 == -(-La // 128) + -(-kv_end // 128), (Lq, La, block, H, max_ctas, item)

@@ -38,7 +38,7 @@ EXPORTS = ("ll_status_str", "ll_cache_create", "ll_cache_destroy", "ll_attend_ch
            "ll_debug_inject_stall", "ll_debug_use_simt", "ll_profile_enable", "ll_profile_read",
            "ll_set_output_dtype", "ll_debug_attend_schedule", "ll_attend_chunk_noalloc",
            "ll_set_chunk_mask", "ll_set_recache_scope", "ll_recache_tokens", "ll_debug_pair_kernel",
-           "ll_debug_poison", "ll_debug_inject_fault", "ll_debug_tile_geom")
+           "ll_debug_poison", "ll_debug_inject_fault")
 LL_KERNEL_ATTEND, LL_KERNEL_PREFILL, LL_KERNEL_COPY = 0, 1, 2
 LL_MASK_CHUNK, LL_MASK_FRAME = 0, 1
 LL_RECACHE_RESIDENT, LL_RECACHE_WINDOW = 0, 1
@@ -89,7 +89,6 @@ def _lib() -> ctypes.CDLL:
             "ll_debug_attend_schedule": (i32, [i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32),
                                                ctypes.POINTER(i32), i32, ctypes.POINTER(i32), i32,
                                                ctypes.POINTER(i32)]),
-            "ll_debug_tile_geom": (i32, [i32, i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32)]),
             "ll_profile_read": (i32, [vp, i32, ctypes.POINTER(i64), ctypes.POINTER(ctypes.c_double)]),
             "ll_attend_chunk_noalloc": (i32, [vp, vp, vp, i32, i64, vp, vp, i32, vp, i32, i32, vp, vp]),
             "ll_set_chunk_mask": (i32, [vp, i32]),
@@ -375,16 +374,6 @@ def ll_debug_attend_schedule(Lq: int, La: int, Lb: int, heads: int, max_ctas: in
         sp.append((splits[i], list(splits[i + 2:i + 2 + cnt])))
         i += 2 + cnt
     return grid.value, out, sp
-
-
-def ll_debug_tile_geom(Lq: int, heads: int, mode: int, item: int, tile: int):
-    """(head, first query row, item count) of query tile `tile` of `item` in the schedule
-    ll_debug_attend_schedule replays (see include/ll.h)."""
-    head, q0 = ctypes.c_int(), ctypes.c_int()
-    n = _lib().ll_debug_tile_geom(Lq, heads, mode, item, tile, ctypes.byref(head), ctypes.byref(q0))
-    if n < 0:
-        raise LLError(LL_ERR_INVALID_ARG, "ll_debug_tile_geom")
-    return head.value, q0.value, n
 
 
 def ll_attend_chunk_noalloc(q, k_cached, v_cached, cached_tokens: int, k, v, out, err_word=None,

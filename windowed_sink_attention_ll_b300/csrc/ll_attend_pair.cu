@@ -661,12 +661,12 @@ cudaError_t launch_attend_bf16_pair(const AttendArgs& a, cudaStream_t stream) {
   static std::atomic<int> attr_done[64];
   if (cudaError_t e = smem_opt_in(attend_pair_kernel, kSmemBytes, attr_done)) return e;
   const int workers = pair_workers(kSmemBytes);
-  plan_items(p.s, a.Lq, a.heads, false);
+  p.s.nqb = (a.Lq + kItemRows - 1) / kItemRows;
   CombineParams cp;
   cp.nsplit = 0;
   if (a.mode == 1) {
     // persistent: one pair per two SMs, items in zigzag rounds (see walker_next)
-    const int items = p.s.items;
+    const int items = p.s.nqb * a.heads;
     p.s.grid = items < workers ? items : workers;
   } else {
     // without scratch for two partial results per pair, no item is split

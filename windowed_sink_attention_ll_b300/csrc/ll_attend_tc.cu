@@ -340,23 +340,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       int u = 0;
       bool ok = true;
       while (ok && walker_next(wk, p.a, p.s, pc, blockIdx.x)) {
-        int hd[NQ], qs[NQ];
-        for (int w = 0; w < NQ; ++w) tile_geom(p.a.mode, p.a.heads, p.s.nqb, p.s.dual, pc.item, w, hd[w], qs[w]);
-        const int nA = (p.a.La + BN - 1) / BN;
-        // a shared last-block item: each query tile has its own head, so its own
-        // K/V stream (per key tile: K of tile 0, K of tile 1, V of tile 0, V of tile 1)
-        const bool dual = hd[1] != hd[0];
+        int head, q0, nA;
+        item_geom(p.a, p.s, pc.item, head, q0, nA);
         // the previous item's Q K^T products must be done with the Q tiles
         if (q_issued > 0 && !(ok = wait(bQempty, (q_issued - 1) & 1, ctl))) break;
         mbar_expect_tx(bQfull, NQ * Cf::kQBytes);
         for (int w = 0; w < NQ; ++w)
           for (int c = 0; c < Cf::kQKChunks; ++c)
-            tma_load_3d(sQ + w * Cf::kQBytes + c * kAtom, &p.tm_q, bQfull, c * Cf::kQKBox, hd[w], qs[w]);
+            tma_load_3d(sQ + w * Cf::kQBytes + c * kAtom, &p.tm_q, bQfull, c * Cf::kQKBox, head, q0 + w * BM);
         ++q_issued;
         for (int j = pc.j0; ok && j < pc.j1; ++j) {
-          for (int ld = 0; ld < (dual ? 4 : 2); ++ld) {
-            const int is_v = dual ? ld >> 1 : ld;
-            const int head = hd[dual ? (ld & 1) : 0];
+          for (int is_v = 0; is_v < 2; ++is_v) {
             const int s = u % NS;
             const int use = u / NS;
             if (use > 0 && !(ok = wait(bKVempty0 + 8 * s, (use - 1) & 1, ctl))) break;
@@ -469,18 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
       bool ok = true;
       while (ok && walker_next(wk, p.a, p.s, pc, blockIdx.x)) {
         const int n = pc.j1 - pc.j0;
-        // ring stages of the item's tiles: K(t), V(t) per key tile; a shared
-        // last-block item (tiles of two heads) has four: K and V of each query tile
-        int hd0, hd1, qr;
-        tile_geom(p.a.mode, p.a.heads, p.s.nqb, p.s.dual, pc.item, 0, hd0, qr);
-        tile_geom(p.a.mode, p.a.heads, p.s.nqb, p.s.dual, pc.item, 1, hd1, qr);
-        const bool dual = hd1 != hd0;
-        const int sp = dual ? 4 : 2;  // stages per key tile
-        const int kb = dual ? 1 : 0;  // stage offset of query tile 1's K
         if (!(ok = __all_sync(0xffffffffu, wait(bQfull, qi & 1, ctl)))) break;
         if (!(ok = __all_sync(0xffffffffu, wait(bKVfull0 + 8 * (u % NS), (u / NS) & 1, ctl)))) break;
-        if (dual && !(ok = __all_sync(0xffffffffu, wait(bKVfull0 + 8 * ((u + 1) % NS), ((u + 1) / NS) & 1, ctl))))
-          break;
         if constexpr (KIND == kTf32) {
           if (!(ok = __all_sync(0xffffffffu, wait(bQsplit, qi & 1, ctl)))) break;
           if (!(ok = __all_sync(0xffffffffu, wait(bKsplit, jt & 1, ctl)))) break;
@@ -488,18 +472,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
         tc_fence_after();
         issue_qk(0, u % NS);
         tc_commit_e(bS0);
-        if (dual) tc_commit_e(bKVempty0 + 8 * (u % NS));
-        issue_qk(1, (u + kb) % NS);
+        issue_qk(1, u % NS);
         tc_commit_e(bS0 + 8);
-        tc_commit_e(bKVempty0 + 8 * ((u + kb) % NS));
+        tc_commit_e(bKVempty0 + 8 * (u % NS));
         if constexpr (KIND == kTf32) tc_commit_e(bKLempty);
         if (n == 1) tc_commit_e(bQempty);
         for (int t = 0; t < n; ++t) {
-          // V of query tiles 0 and 1 at key tile t; K of both at key tile t + 1
-          const int uv = u + sp * t + (dual ? 2 : 1), sv = uv % NS;
-          const int uv1 = uv + (dual ? 1 : 0), sv1 = uv1 % NS;
-          const int uk = u + sp * (t + 1), sk = uk % NS;
-          const int uk1 = uk + kb, sk1 = uk1 % NS;
+          const int uv = u + 2 * t + 1, sv = uv % NS;
+          const int uk = u + 2 * t + 2, sk = uk % NS;
           const bool more = t + 1 < n;
           if (!(ok = __all_sync(0xffffffffu, wait(bKVfull0 + 8 * sv, (uv / NS) & 1, ctl)))) break;
           if (!(ok = __all_sync(0xffffffffu, wait(bP0, (jt + t) & 1, ctl)))) break;
@@ -508,7 +488,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
           }
           // e4m3 V: the fp16 buffer of V tile jt + t
           const int pvs = KIND == kE4m3KV ? ((jt + t) & 1) : sv;
-          const int pvs1 = KIND == kE4m3KV ? ((jt + t) & 1) : sv1;
           if constexpr (KIND == kE4m3KV) {
             if (!(ok = __all_sync(0xffffffffu, wait(bWfull0 + 8 * pvs, ((jt + t) >> 1) & 1, ctl)))) break;
           }
@@ -519,7 +498,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
           if (!(ok = __all_sync(0xffffffffu, wait(bP0 + 16, (jt + t) & 1, ctl)))) break;
           tc_fence_after();
           issue_pv(0, pvs, 1, true);
-          if (dual) tc_commit_e(bKVempty0 + 8 * sv);
           if (more) {
             if (!(ok = __all_sync(0xffffffffu, wait(bKVfull0 + 8 * sk, (uk / NS) & 1, ctl)))) break;
             if constexpr (KIND == kTf32) {
@@ -528,33 +506,27 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
             tc_fence_after();
             issue_qk(0, sk);
             tc_commit_e(bS0);
-            if (dual) tc_commit_e(bKVempty0 + 8 * sk);
           }
-          if (dual && !(ok = __all_sync(0xffffffffu, wait(bKVfull0 + 8 * sv1, (uv1 / NS) & 1, ctl)))) break;
           if (!(ok = __all_sync(0xffffffffu, wait(bP0 + 8, (jt + t) & 1, ctl)))) break;
           tc_fence_after();
-          issue_pv(1, pvs1, 0, t > 0);
+          issue_pv(1, pvs, 0, t > 0);
           if (!(ok = __all_sync(0xffffffffu, wait(bP0 + 24, (jt + t) & 1, ctl)))) break;
           tc_fence_after();
-          issue_pv(1, pvs1, 1, true);
-          tc_commit_e(bKVempty0 + 8 * sv1);
+          issue_pv(1, pvs, 1, true);
+          tc_commit_e(bKVempty0 + 8 * sv);
           if constexpr (KIND == kTf32) tc_commit_e(bVTempty);
           if constexpr (KIND == kE4m3KV) tc_commit_e(bWempty0 + 8 * pvs);
           if (more) {
-            if (dual) {
-              if (!(ok = __all_sync(0xffffffffu, wait(bKVfull0 + 8 * sk1, (uk1 / NS) & 1, ctl)))) break;
-              tc_fence_after();
-            }
-            issue_qk(1, sk1);
+            issue_qk(1, sk);
             tc_commit_e(bS0 + 8);
-            tc_commit_e(bKVempty0 + 8 * sk1);
+            tc_commit_e(bKVempty0 + 8 * sk);
             if constexpr (KIND == kTf32) tc_commit_e(bKLempty);
             if (t + 2 == n) tc_commit_e(bQempty);
           }
         }
         if (!ok) break;
         tc_commit_e(bOfull);
-        u += sp * n;
+        u += 2 * n;
         jt += n;
         ++qi;
       }
@@ -698,10 +670,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_tc_kernel(const __grid_con
     int qi = 0, jt = 0;
     bool ok = true;
     while (ok && walker_next(wk, p.a, p.s, pc, blockIdx.x)) {
-      int head, q0;
-      tile_geom(a.mode, a.heads, p.s.nqb, p.s.dual, pc.item, w, head, q0);
-      const int nA = (a.La + BN - 1) / BN;
-      const int qrow = q0 + row;
+      int head, q0, nA;
+      item_geom(p.a, p.s, pc.item, head, q0, nA);
+      const int qrow = q0 + w * BM + row;
       int row_end = a.Lb;
       if (a.mode != 0) {
         const long long e = ((long long)qrow / a.block_tokens + 1) * a.block_tokens;
@@ -958,14 +929,12 @@ cudaError_t launch_tc(const AttendArgs& a, cudaStream_t stream) {
       !encode_cache(&p.tm_kc, a.kc, a.La, a.heads, D, a.cache_head_elems, BN, qk) ||
       !encode_cache(&p.tm_vc, a.vc, a.La, a.heads, D, a.cache_head_elems, BN, ve))
     return cudaErrorInvalidValue;
-  // shared last-block items where the K/V tiles come straight from the ring (bf16,
-  // e4m3 keys); the fp32 and e4m3-value forms prepare one V (and K) tile at a time
-  plan_items(p.s, a.Lq, a.heads, KIND == kBf16 || KIND == kE4m3);
+  p.s.nqb = (a.Lq + NQ * BM - 1) / (NQ * BM);
   CombineParams cp;
   cp.nsplit = 0;
   if (a.mode == 1) {
     // persistent: one CTA per SM, items in zigzag rounds (see walker_next)
-    const int items = p.s.items;
+    const int items = p.s.nqb * a.heads;
     const int sms = sm_count();
     p.s.grid = items < sms ? items : sms;
   } else {
@@ -1010,11 +979,11 @@ int attend_schedule_dump(int Lq, int La, int Lb, int heads, int max_ctas, int mo
   a.block_tokens = block_tokens;
   Sched sc;
   std::memset(&sc, 0, sizeof(sc));
-  plan_items(sc, Lq, heads, true);  // the schedule of the bf16 one-CTA kernel
+  sc.nqb = (Lq + kItemRows - 1) / kItemRows;
   CombineParams cp;
   cp.nsplit = 0;
   if (mode == 1) {
-    const int items = sc.items;
+    const int items = sc.nqb * heads;
     sc.grid = items < max_ctas ? items : max_ctas;
   } else {
     plan_attend(a, sc, cp, max_ctas);
@@ -1050,17 +1019,6 @@ int attend_schedule_dump(int Lq, int La, int Lb, int heads, int max_ctas, int mo
   }
   *split_ints = m;
   return n / 6;
-}
-
-int attend_tile_geom(int Lq, int heads, int mode, int item, int tile, int* head, int* q0) {
-  using namespace tc;
-  if (Lq < 1 || heads < 1 || tile < 0 || tile > 1 || !head || !q0) return -1;
-  Sched sc;
-  std::memset(&sc, 0, sizeof(sc));
-  plan_items(sc, Lq, heads, true);
-  if (item < 0 || item >= sc.items) return -1;
-  tile_geom(mode, heads, sc.nqb, sc.dual, item, tile, *head, *q0);
-  return sc.items;
 }
 
 cudaError_t launch_attend_bf16_tc(const AttendArgs& a, cudaStream_t stream) {

@@ -699,11 +699,6 @@ int ll_debug_attend_schedule(int Lq, int La, int Lb, int heads, int max_ctas, in
                                   split_cap, split_ints);
 }
 
-int ll_debug_tile_geom(int Lq, int heads, int mode, int item, int tile, int* head, int* q0) {
-  if (mode < 0 || mode > 2) return -1;
-  return ll::attend_tile_geom(Lq, heads, mode, item, tile, head, q0);
-}
-
 ll_status ll_debug_use_simt(ll_cache* c, int enable) {
   if (!c) return LL_ERR_INVALID_ARG;
   c->use_simt = enable ? 1 : 0;

@@ -94,9 +94,6 @@ int attend_scratch_slots_wanted();
 // as (item, parts, slots...).
 int attend_schedule_dump(int Lq, int La, int Lb, int heads, int max_ctas, int mode, int block_tokens, int* grid,
                          int* out, int cap, int* splits, int split_cap, int* split_ints);
-// Host replay of the item geometry of the same kernel (tests): head and first query
-// row of query tile `tile` of `item`; returns the launch's item count, -1 for bad arguments.
-int attend_tile_geom(int Lq, int heads, int mode, int item, int tile, int* head, int* q0);
 cudaError_t launch_attend_simt(const AttendArgs& a, int elem_bytes, cudaStream_t stream);
 
 void count_launch();

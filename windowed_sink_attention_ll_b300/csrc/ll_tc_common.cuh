@@ -249,17 +249,8 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
 // blocks of keys); round r gives worker c item r*grid + c (r even) or
 // r*grid + grid - 1 - c (r odd), which keeps every worker's total within one
 // item of the mean without splitting any item.
-// Shared last blocks (`dual`, one-CTA kernel, bf16 or e4m3 keys): when the last
-// query block of a head holds at most 128 rows, its item would carry one query
-// tile and an empty one, at about the cost of a full item.  Instead the last
-// blocks of heads 2i and 2i+1 share one item, query tile w taking head 2i + w
-// (each tile with its own K/V stream); with an odd head count the last head's
-// block stays alone.  Attend modes number such items after all others; prefill
-// numbers them first (they are the longest).
 struct Sched {
   int nqb;               // query blocks of 256 rows per head
-  int items;             // work items
-  int dual;              // 1: heads share the items of their last (short) query blocks
   int nkv;               // attend: key tiles per item
   int grid;              // workers launched
   int rounds;            // attend: whole-item rounds
@@ -291,51 +282,6 @@ __host__ __device__ __forceinline__ void walker_init(Walker& w, const AttendArgs
   w.it = w.begin;
 }
 
-// Query block of a prefill item (numbered longest first; shared last blocks first).
-__host__ __device__ __forceinline__ int prefill_item_qb(int heads, int nqb, int dual, int item) {
-  const int nd = dual ? (heads + 1) / 2 : 0;
-  return item < nd ? nqb - 1 : nqb - 1 - dual - (item - nd) / heads;
-}
-
-// Query tile w (0 or 1) of a work item: its head and first query row.  A tile of
-// an item of one head covers rows [q0, q0 + 128) of the item's 256-row block; the
-// two tiles of a shared last-block item belong to two heads and start at the same
-// row; a tile past the head's last row (short last block, not shared) is skipped
-// by every consumer of its rows.
-__host__ __device__ __forceinline__ void tile_geom(int mode, int heads, int nqb, int dual, int item, int w,
-                                                   int& head, int& q0) {
-  const int per_head = nqb - dual;  // items that belong to one head alone
-  int qb, pair = -1;
-  if (mode != 1) {
-    if (item < heads * per_head) {
-      head = item / per_head;
-      qb = item - head * per_head;
-    } else {
-      pair = item - heads * per_head;
-      qb = nqb - 1;
-    }
-  } else {
-    const int nd = dual ? (heads + 1) / 2 : 0;
-    qb = prefill_item_qb(heads, nqb, dual, item);
-    if (item < nd) {
-      pair = item;
-    } else {
-      const int i = item - nd;
-      head = i - (i / heads) * heads;
-    }
-  }
-  if (pair >= 0) {
-    const int h = 2 * pair + w;
-    if (h < heads) {
-      head = h;
-      q0 = qb * kItemRows;
-      return;
-    }
-    head = 2 * pair;  // odd head count: the last head's short block alone
-  }
-  q0 = qb * kItemRows + w * (kItemRows / 2);
-}
-
 // Key tiles a prefill item of query block qb needs: every cached tile (source A,
 // fully visible) and the fresh tiles up to the end of the block of its last row.
 __host__ __device__ __forceinline__ int prefill_nkv(const AttendArgs& a, int qb) {
@@ -351,14 +297,14 @@ __host__ __device__ __forceinline__ bool walker_next(Walker& w, const AttendArgs
   if (w.prefill) {
     // items come longest first; round r hands them out left to right (even r) or
     // right to left (odd r), so each worker's total stays close to the mean
-    const int items = s.items;
+    const int items = s.nqb * a.heads;
     while (w.r * s.grid < items) {
       const int r = w.r++;
       const int item = r * s.grid + ((r & 1) ? s.grid - 1 - cta : cta);
       if (item >= items) continue;
       pc.item = item;
       pc.j0 = 0;
-      pc.j1 = prefill_nkv(a, prefill_item_qb(a.heads, s.nqb, s.dual, item));
+      pc.j1 = prefill_nkv(a, s.nqb - 1 - item / a.heads);
       pc.partial = 0;
       pc.slot = 0;
       return true;
@@ -388,20 +334,18 @@ __host__ __device__ __forceinline__ bool walker_next(Walker& w, const AttendArgs
   return true;
 }
 
-// head and first query row of an item's first tile, and the cache-tile count
+// head, first query row and cache-tile count of an item
 __device__ __forceinline__ void item_geom(const AttendArgs& a, const Sched& s, int item, int& head, int& q0,
                                           int& nA) {
-  tile_geom(a.mode, a.heads, s.nqb, s.dual, item, 0, head, q0);
+  if (a.mode != 1) {
+    head = item / s.nqb;
+    q0 = (item - head * s.nqb) * kItemRows;
+  } else {
+    const int qb = s.nqb - 1 - item / a.heads;
+    head = item - (item / a.heads) * a.heads;
+    q0 = qb * kItemRows;
+  }
   nA = (a.La + kKeyTile - 1) / kKeyTile;
-}
-
-// Items of a launch over Lq query rows and `heads` heads; sets s.nqb, s.dual, s.items.
-// Shared last blocks only where the caller's kernel supports them.
-__host__ __device__ __forceinline__ void plan_items(Sched& s, int Lq, int heads, bool allow_dual) {
-  s.nqb = (Lq + kItemRows - 1) / kItemRows;
-  const int last_rows = Lq - (s.nqb - 1) * kItemRows;
-  s.dual = (allow_dual && heads >= 2 && s.nqb >= 1 && last_rows <= kItemRows / 2) ? 1 : 0;
-  s.items = heads * (s.nqb - s.dual) + (s.dual ? (heads + 1) / 2 : 0);
 }
 
 struct CombineParams {
@@ -411,7 +355,6 @@ struct CombineParams {
   int nqb;
   int Lq;
   int heads;
-  int dual;  // shared last-block items (see tile_geom)
   int out_f32;
   int nsplit;
   int item[kMaxSplit];
@@ -422,7 +365,7 @@ struct CombineParams {
 // Schedule of an attend launch with at most max_workers workers (see "Work
 // schedule"); fills s and the split list.
 inline void plan_attend(const AttendArgs& a, Sched& s, CombineParams& cp, int max_workers) {
-  const int items = s.items;
+  const int items = s.nqb * a.heads;
   s.nkv = (a.La + kKeyTile - 1) / kKeyTile + (a.Lb + kKeyTile - 1) / kKeyTile;
   int g = max_workers < kMaxSplit ? max_workers : kMaxSplit;
   if (g > items) g = items;
@@ -467,9 +410,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const __grid_constant__ Co
   const int r = blockIdx.y * 8 + (threadIdx.x >> 5);  // row within the item's 256 query rows
   const int lane = threadIdx.x & 31;
   const int item = c.item[k];
-  int head, q0;
-  tile_geom(0, c.heads, c.nqb, c.dual, item, r / (kItemRows / 2), head, q0);
-  const int qrow = q0 + r % (kItemRows / 2);
+  const int head = item / c.nqb;
+  const int qrow = (item - head * c.nqb) * kItemRows + r;
   if (qrow >= c.Lq) return;
   const size_t rows_all = (size_t)2 * c.grid * kItemRows;
   const float* pm = c.part + rows_all * D;
@@ -510,7 +452,6 @@ inline cudaError_t launch_combine(CombineParams& cp, const AttendArgs& a, const 
   cp.nqb = s.nqb;
   cp.Lq = a.Lq;
   cp.heads = a.heads;
-  cp.dual = s.dual;
   cp.out_f32 = a.out_f32;
   const cudaError_t e =
       launch_dependent(combine_kernel<D>, dim3((unsigned)cp.nsplit, kItemRows / 8), dim3(256), 0, stream, cp);
